@@ -1,0 +1,147 @@
+"""Python binding of libqgemm (the C ABI in include/qgemm.h).
+
+Argument marshalling only: every function takes torch tensors that already live
+on the GPU, derives sizes from their shapes, passes raw device pointers and the
+current CUDA stream to the C entry point of the same name, and raises
+``QGError`` on a non-zero status. All arithmetic happens in the CUDA kernels of
+the shared library; there is no other implementation to fall back to, and
+loading fails loudly if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+Q4_0 = 2
+Q8_0 = 8
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqgemm.so")
+
+EXPORTS = ("qg_status_str", "qgemv_q4_0", "qgemv_q8_0", "qgemm_cols", "qffn_gate_up_silu",
+           "qmoe_workspace_bytes", "qmoe_experts", "qrepack", "qg_kernel_launches")
+
+STATUS = {0: "QG_OK", 1: "QG_ERR_NULL", 2: "QG_ERR_SHAPE", 3: "QG_ERR_ALIGN", 4: "QG_ERR_TYPE",
+          5: "QG_ERR_WORKSPACE", 6: "QG_ERR_CUDA", 7: "QG_ERR_ALIAS"}
+
+
+class QGError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {STATUS.get(status, status)} ({msg})")
+        self.status = status
+
+
+class QGExpert(C.Structure):
+    _fields_ = [("qg", C.c_void_p), ("sg", C.c_void_p), ("qu", C.c_void_p),
+                ("su", C.c_void_p), ("qd", C.c_void_p), ("sd", C.c_void_p)]
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libqgemm.so (built by ``gemm_q4_q8_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"libqgemm.so not built ({path}); run gemm_q4_q8_gb300.build.build()")
+    L = C.CDLL(path)
+    vp, i32, sz = C.c_void_p, C.c_int, C.c_size_t
+    L.qg_status_str.argtypes = [i32]
+    L.qg_status_str.restype = C.c_char_p
+    gemv = [vp, vp, i32, i32, vp, i32, vp, vp, vp]
+    L.qgemv_q4_0.argtypes = gemv
+    L.qgemv_q8_0.argtypes = gemv
+    L.qgemm_cols.argtypes = [i32] + gemv
+    L.qffn_gate_up_silu.argtypes = [i32, vp, vp, vp, vp, i32, i32, vp, i32, vp, vp]
+    L.qmoe_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    L.qmoe_workspace_bytes.restype = sz
+    L.qmoe_experts.argtypes = [i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32,
+                               C.POINTER(QGExpert), vp, i32, vp, vp, vp, sz, vp, vp, vp]
+    L.qrepack.argtypes = [i32, vp, i32, i32, vp, vp, vp]
+    L.qg_kernel_launches.argtypes = []
+    L.qg_kernel_launches.restype = C.c_uint64
+    for f in EXPORTS:
+        if f not in ("qg_status_str", "qmoe_workspace_bytes", "qg_kernel_launches"):
+            getattr(L, f).restype = i32
+    _lib = L
+    return L
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise QGError(fn, st, load().qg_status_str(st).decode())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def qgemv_q4_0(nib, scl, x, y, y0=None, stream=None):
+    """y[c] = y0[c] + W x[c]; nib uint8 [rows, k/2], scl f16-bits [rows, k/32],
+    x f16 [ncols, k] (1..8 columns), y / y0 f32 [ncols, rows]."""
+    rows, k = scl.shape[0], scl.shape[1] * 32
+    _check("qgemv_q4_0", load().qgemv_q4_0(_ptr(nib), _ptr(scl), rows, k, _ptr(x), x.shape[0],
+                                           _ptr(y0), _ptr(y), _stream(stream)))
+
+
+def qgemv_q8_0(qs, scl, x, y, y0=None, stream=None):
+    """As qgemv_q4_0 with int8 quants qs [rows, k]."""
+    rows, k = scl.shape[0], scl.shape[1] * 32
+    _check("qgemv_q8_0", load().qgemv_q8_0(_ptr(qs), _ptr(scl), rows, k, _ptr(x), x.shape[0],
+                                           _ptr(y0), _ptr(y), _stream(stream)))
+
+
+def qgemm_cols(qtype, q, scl, x, y, y0=None, stream=None):
+    """y[c] = y0[c] + W x[c] for 1..16 columns."""
+    rows, k = scl.shape[0], scl.shape[1] * 32
+    _check("qgemm_cols", load().qgemm_cols(int(qtype), _ptr(q), _ptr(scl), rows, k, _ptr(x),
+                                           x.shape[0], _ptr(y0), _ptr(y), _stream(stream)))
+
+
+def qffn_gate_up_silu(qtype, qg, sg, qu, su, x, h, stream=None):
+    """h[c] = f16(SiLU(Wg x[c]) * (Wu x[c])), h f16 [ncols, rows], 1..16 columns."""
+    rows, k = sg.shape[0], sg.shape[1] * 32
+    _check("qffn_gate_up_silu",
+           load().qffn_gate_up_silu(int(qtype), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), rows, k,
+                                    _ptr(x), x.shape[0], _ptr(h), _stream(stream)))
+
+
+def qmoe_workspace_bytes(n_expert, ffn, hidden, ncols, topk) -> int:
+    return int(load().qmoe_workspace_bytes(n_expert, ffn, hidden, ncols, topk))
+
+
+def qmoe_experts(qtype, qg, sg, qu, su, qd, sd, n_expert, ffn, hidden, ids, rw, x, y,
+                 ws, y0=None, shared=None, err_flag=None, uniq_ids_out=None, stream=None):
+    """Stacked-expert MoE layer; ``shared`` is None or a dict with keys
+    qg, sg, qu, su, qd, sd (device tensors)."""
+    sh = None
+    if shared is not None:
+        sh = C.pointer(QGExpert(*[_ptr(shared[n]) for n in ("qg", "sg", "qu", "su", "qd", "sd")]))
+    ncols, topk = ids.shape
+    _check("qmoe_experts",
+           load().qmoe_experts(int(qtype), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(qd),
+                               _ptr(sd), n_expert, ffn, hidden, _ptr(ids), _ptr(rw), topk, sh,
+                               _ptr(x), ncols, _ptr(y0), _ptr(y), _ptr(ws),
+                               ws.numel() * ws.element_size(), _ptr(err_flag),
+                               _ptr(uniq_ids_out), _stream(stream)))
+
+
+def qg_kernel_launches() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(load().qg_kernel_launches())
+
+
+def qrepack(qtype, gguf, rows, k, q_out, scl_out, stream=None):
+    """GGUF interleaved blocks (device bytes) -> quant and scale arrays."""
+    _check("qrepack", load().qrepack(int(qtype), _ptr(gguf), rows, k, _ptr(q_out), _ptr(scl_out),
+                                     _stream(stream)))

@@ -1,0 +1,210 @@
+// qg_api.cu -- the C ABI of libqgemm: argument checks on the host, then
+// dispatch to the kernels on the caller's stream. Nothing here allocates.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "qg_internal.h"
+#include "qgemm.h"
+
+namespace qg {
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace qg
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool valid_type(int t) { return t == QG_Q4_0 || t == QG_Q8_0; }
+
+// Partial overlap of two byte ranges (identical start is allowed by the caller).
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+qg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QG_OK : QG_ERR_CUDA; }
+
+// Common checks of a (rows x k) matrix product with ncols input columns.
+qg_status check_matmul(int t, const void* q, const uint16_t* scl, int rows, int k,
+                       const uint16_t* x, int ncols, int max_cols, const float* y0,
+                       const void* out, size_t out_elem) {
+  if (!valid_type(t)) return QG_ERR_TYPE;
+  if (rows < 0 || k <= 0 || (k % 32) != 0 || ncols < 1 || ncols > max_cols) return QG_ERR_SHAPE;
+  if (rows == 0) return QG_OK;
+  if (!q || !scl || !x || !out) return QG_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(scl, 16) || !aligned(x, 16) || !aligned(out, out_elem) ||
+      (y0 && !aligned(y0, 4)))
+    return QG_ERR_ALIGN;
+  if (y0 && y0 != out) {
+    const size_t n = (size_t)ncols * rows * sizeof(float);
+    if (overlaps(y0, n, out, n)) return QG_ERR_ALIAS;
+  }
+  return QG_OK;
+}
+
+// Device readiness (a device must be present and current).
+qg_status check_device() { return qg::device_sm_count() > 0 ? QG_OK : QG_ERR_CUDA; }
+
+qg_status gemv_any(int t, const void* q, const uint16_t* scl, int rows, int k,
+                   const uint16_t* x, int ncols, const float* y0, float* y, cudaStream_t s,
+                   int max_cols) {
+  qg_status st = check_matmul(t, q, scl, rows, k, x, ncols, max_cols, y0, y, 4);
+  if (st != QG_OK || rows == 0) return st;
+  if ((st = check_device()) != QG_OK) return st;
+  if (qg::tc_supported(t, ncols, false, rows, k))
+    return from_cuda(qg::tc_gemm(t, q, scl, nullptr, nullptr, rows, k, x, ncols, y0, y, nullptr, s));
+  // CUDA-core path, at most 8 columns per launch
+  for (int c0 = 0; c0 < ncols; c0 += 8) {
+    const int nc = ncols - c0 < 8 ? ncols - c0 : 8;
+    cudaError_t e = qg::cc_gemv(t, q, scl, rows, k, x + (size_t)c0 * k, nc,
+                                y0 ? y0 + (size_t)c0 * rows : nullptr, y + (size_t)c0 * rows, s);
+    if (e != cudaSuccess) return QG_ERR_CUDA;
+  }
+  return QG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qg_status_str(qg_status s) {
+  switch (s) {
+    case QG_OK: return "ok";
+    case QG_ERR_NULL: return "a required pointer is NULL";
+    case QG_ERR_SHAPE: return "invalid shape (k must be a positive multiple of 32; rows >= 0; ncols/topk/n_expert in range)";
+    case QG_ERR_ALIGN: return "misaligned pointer (quants, scales, x: 16 bytes; y, y0: 4 bytes; h: 2 bytes)";
+    case QG_ERR_TYPE: return "unknown quant type (expected Q4_0=2 or Q8_0=8)";
+    case QG_ERR_WORKSPACE: return "workspace missing or smaller than qmoe_workspace_bytes()";
+    case QG_ERR_CUDA: return "CUDA runtime error";
+    case QG_ERR_ALIAS: return "y0 partially overlaps y";
+  }
+  return "unknown status";
+}
+
+qg_status qgemv_q4_0(const uint8_t* nib, const uint16_t* scl, int rows, int k,
+                     const uint16_t* x, int ncols, const float* y0, float* y,
+                     cudaStream_t stream) {
+  return gemv_any(QG_Q4_0, nib, scl, rows, k, x, ncols, y0, y, stream, 8);
+}
+
+qg_status qgemv_q8_0(const int8_t* qs, const uint16_t* scl, int rows, int k,
+                     const uint16_t* x, int ncols, const float* y0, float* y,
+                     cudaStream_t stream) {
+  return gemv_any(QG_Q8_0, qs, scl, rows, k, x, ncols, y0, y, stream, 8);
+}
+
+qg_status qgemm_cols(qg_type t, const void* q, const uint16_t* scl, int rows, int k,
+                     const uint16_t* x, int ncols, const float* y0, float* y,
+                     cudaStream_t stream) {
+  return gemv_any((int)t, q, scl, rows, k, x, ncols, y0, y, stream, 16);
+}
+
+qg_status qffn_gate_up_silu(qg_type t, const void* qg, const uint16_t* sg, const void* qu,
+                            const uint16_t* su, int rows, int k, const uint16_t* x,
+                            int ncols, uint16_t* h, cudaStream_t stream) {
+  qg_status st = check_matmul((int)t, qg, sg, rows, k, x, ncols, 16, nullptr, h, 2);
+  if (st != QG_OK || rows == 0) return st;
+  if (!qu || !su) return QG_ERR_NULL;
+  if (!aligned(qu, 16) || !aligned(su, 16)) return QG_ERR_ALIGN;
+  if ((st = check_device()) != QG_OK) return st;
+  if (qg::tc_supported((int)t, ncols, true, rows, k))
+    return from_cuda(qg::tc_gemm((int)t, qg, sg, qu, su, rows, k, x, ncols, nullptr, nullptr, h, stream));
+  for (int c0 = 0; c0 < ncols; c0 += 8) {
+    const int nc = ncols - c0 < 8 ? ncols - c0 : 8;
+    cudaError_t e = qg::cc_gate_up_silu((int)t, qg, sg, qu, su, rows, k, x + (size_t)c0 * k, nc,
+                                        h + (size_t)c0 * rows, stream);
+    if (e != cudaSuccess) return QG_ERR_CUDA;
+  }
+  return QG_OK;
+}
+
+size_t qmoe_workspace_bytes(int n_expert, int ffn, int hidden, int ncols, int topk) {
+  if (n_expert < 1 || ffn <= 0 || hidden <= 0 || ncols < 1 || ncols > 8 || topk < 1 || topk > 16)
+    return 0;
+  return qg::moe_ws_bytes(n_expert, ffn, hidden, ncols, topk);
+}
+
+qg_status qmoe_experts(qg_type t, const void* qg, const uint16_t* sg, const void* qu,
+                       const uint16_t* su, const void* qd, const uint16_t* sd,
+                       int n_expert, int ffn, int hidden, const int32_t* ids,
+                       const float* rw, int topk, const qg_expert* shared,
+                       const uint16_t* x, int ncols, const float* y0, float* y,
+                       void* ws, size_t ws_bytes, int32_t* err_flag,
+                       int32_t* uniq_ids_out, cudaStream_t stream) {
+  if (!valid_type((int)t)) return QG_ERR_TYPE;
+  if (n_expert < 1 || ffn <= 0 || hidden <= 0 || (ffn % 32) || (hidden % 32) || ncols < 1 ||
+      ncols > 8 || topk < 1 || topk > 16 || !qg::moe_shape_supported(ffn, hidden, ncols))
+    return QG_ERR_SHAPE;
+  if (!qg || !sg || !qu || !su || !qd || !sd || !ids || !rw || !x || !y) return QG_ERR_NULL;
+  const void* p16[] = {qg, sg, qu, su, qd, sd, x};
+  for (const void* p : p16)
+    if (!aligned(p, 16)) return QG_ERR_ALIGN;
+  if (!aligned(ids, 4) || !aligned(rw, 4) || !aligned(y, 4) || (y0 && !aligned(y0, 4)) ||
+      (err_flag && !aligned(err_flag, 4)) || (uniq_ids_out && !aligned(uniq_ids_out, 4)))
+    return QG_ERR_ALIGN;
+  if (shared) {
+    if (!shared->qg || !shared->sg || !shared->qu || !shared->su || !shared->qd || !shared->sd)
+      return QG_ERR_NULL;
+    const void* s16[] = {shared->qg, shared->sg, shared->qu, shared->su, shared->qd, shared->sd};
+    for (const void* p : s16)
+      if (!aligned(p, 16)) return QG_ERR_ALIGN;
+  }
+  if (y0 && y0 != y) {
+    const size_t n = (size_t)ncols * hidden * sizeof(float);
+    if (overlaps(y0, n, y, n)) return QG_ERR_ALIAS;
+  }
+  const size_t need = qg::moe_ws_bytes(n_expert, ffn, hidden, ncols, topk);
+  if (!ws || ws_bytes < need) return QG_ERR_WORKSPACE;
+  if (!aligned(ws, 16)) return QG_ERR_ALIGN;
+  qg_status st = check_device();
+  if (st != QG_OK) return st;
+  qg::MoeArgs a{};
+  a.qt = (int)t;
+  a.qg = qg; a.qu = qu; a.qd = qd; a.sg = sg; a.su = su; a.sd = sd;
+  a.n_expert = n_expert; a.ffn = ffn; a.hidden = hidden;
+  a.ids = ids; a.rw = rw; a.topk = topk;
+  a.has_shared = shared != nullptr;
+  if (shared) {
+    a.sqg = shared->qg; a.squ = shared->qu; a.sqd = shared->qd;
+    a.ssg = shared->sg; a.ssu = shared->su; a.ssd = shared->sd;
+  }
+  a.x = x; a.ncols = ncols; a.y0 = y0; a.y = y;
+  a.ws = ws; a.err_flag = err_flag; a.uniq_out = uniq_ids_out;
+  return from_cuda(qg::moe_forward(a, stream));
+}
+
+qg_status qrepack(qg_type t, const void* gguf, int rows, int k, void* q_out,
+                  uint16_t* scl_out, cudaStream_t stream) {
+  if (!valid_type((int)t)) return QG_ERR_TYPE;
+  if (rows < 0 || k <= 0 || (k % 32) != 0) return QG_ERR_SHAPE;
+  if (rows == 0) return QG_OK;
+  if (!gguf || !q_out || !scl_out) return QG_ERR_NULL;
+  if (!aligned(gguf, 2) || !aligned(q_out, 16) || !aligned(scl_out, 16)) return QG_ERR_ALIGN;
+  qg_status st = check_device();
+  if (st != QG_OK) return st;
+  return from_cuda(qg::repack_launch((int)t, gguf, rows, k, q_out, scl_out, stream));
+}
+
+uint64_t qg_kernel_launches(void) { return qg::g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

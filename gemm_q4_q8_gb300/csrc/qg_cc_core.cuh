@@ -1,0 +1,144 @@
+// qg_cc_core.cuh -- CUDA-core building blocks: per-block loads, exact
+// dequantisation dot products and x staging, shared by the GEMV and MoE kernels.
+#pragma once
+#include "qg_common.cuh"
+
+namespace qg {
+
+// One block's quants for one row.
+template <int QT> struct Blk;
+template <> struct Blk<T_Q4_0> {
+  uint4 a;
+  __device__ __forceinline__ void load(const uint8_t* p) { a = ld_stream16(p); }
+};
+template <> struct Blk<T_Q8_0> {
+  uint4 a, b;
+  __device__ __forceinline__ void load(const uint8_t* p) {
+    a = ld_stream16(p);
+    b = ld_stream16(p + 16);
+  }
+};
+
+// Dot of one block of one row with one column's staged x (32 floats in the
+// consumption order of the quant type). Returns the unscaled block sum.
+__device__ __forceinline__ float blk_dot(const Blk<T_Q4_0>& q, const float2 (&xr)[16]) {
+  float2 acc = make_float2(0.f, 0.f);
+  const uint32_t w[4] = {q.a.x, q.a.y, q.a.z, q.a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    Q4Word d = dequant_q4_word(w[i]);
+    acc = fma2(d.p0, xr[4 * i + 0], acc);
+    acc = fma2(d.p1, xr[4 * i + 1], acc);
+    acc = fma2(d.p2, xr[4 * i + 2], acc);
+    acc = fma2(d.p3, xr[4 * i + 3], acc);
+  }
+  return acc.x + acc.y;
+}
+__device__ __forceinline__ float blk_dot(const Blk<T_Q8_0>& q, const float2 (&xr)[16]) {
+  float2 acc = make_float2(0.f, 0.f);
+  const uint32_t w[8] = {q.a.x, q.a.y, q.a.z, q.a.w, q.b.x, q.b.y, q.b.z, q.b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    Q8Word d = dequant_q8_word(w[i]);
+    acc = fma2(d.p0, xr[2 * i + 0], acc);
+    acc = fma2(d.p1, xr[2 * i + 1], acc);
+  }
+  return acc.x + acc.y;
+}
+
+// Dequantised block (for the multi-column baseline: dequantise once, reuse for
+// every column).
+__device__ __forceinline__ void blk_dequant(const Blk<T_Q4_0>& q, float2 (&wv)[16]) {
+  const uint32_t w[4] = {q.a.x, q.a.y, q.a.z, q.a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    Q4Word d = dequant_q4_word(w[i]);
+    wv[4 * i + 0] = d.p0; wv[4 * i + 1] = d.p1; wv[4 * i + 2] = d.p2; wv[4 * i + 3] = d.p3;
+  }
+}
+__device__ __forceinline__ void blk_dequant(const Blk<T_Q8_0>& q, float2 (&wv)[16]) {
+  const uint32_t w[8] = {q.a.x, q.a.y, q.a.z, q.a.w, q.b.x, q.b.y, q.b.z, q.b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    Q8Word d = dequant_q8_word(w[i]);
+    wv[2 * i + 0] = d.p0; wv[2 * i + 1] = d.p1;
+  }
+}
+__device__ __forceinline__ float wv_dot(const float2 (&wv)[16], const float2 (&xr)[16]) {
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    a0 = fma2(wv[i], xr[i], a0);
+    a1 = fma2(wv[i + 1], xr[i + 1], a1);
+  }
+  return (a0.x + a0.y) + (a1.x + a1.y);
+}
+
+__device__ __forceinline__ void load_x16(const float* p, float2 (&xr)[16]) {
+  const float4* p4 = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float4 v = p4[i];
+    xr[2 * i] = make_float2(v.x, v.y);
+    xr[2 * i + 1] = make_float2(v.z, v.w);
+  }
+}
+
+// Stage x[c][kb0*32 .. kb1*32) of the selected columns into shared memory as
+// f32 in the consumption order of QT.
+template <int QT, int NC>
+__device__ __forceinline__ void stage_x(float* xs, int xstride, const __half* x, int k,
+                                        const int (&cols)[NC], int kb0, int kb1) {
+  const int n = (kb1 - kb0) * QK;
+  for (int c = 0; c < NC; ++c) {
+    const __half* xc = x + (size_t)cols[c] * k + (size_t)kb0 * QK;
+    float* dst = xs + c * xstride;
+    for (int s = threadIdx.x; s < n; s += blockDim.x) {
+      const int b = s >> 5, j = s & 31;
+      float v;
+      if (QT == T_Q4_0) {
+        v = __half2float(xc[b * QK + q4_xorder_elem(j)]) * q4_xorder_scale(j);
+      } else {
+        v = __half2float(xc[s]);
+      }
+      dst[s] = v;
+    }
+  }
+}
+
+
+// One warp: 1-column dot of RW rows (and of a second matrix when DUAL) over
+// the blocks [kb0, kb1) of the staged x chunk; lane l takes blocks kb0+l,
+// kb0+l+32, ... Accumulates per-row totals (block scales applied per block).
+template <int QT, int RW, bool DUAL>
+__device__ __forceinline__ void cc_rowdot_1col(const uint8_t* __restrict__ qa,
+                                               const uint16_t* __restrict__ sa,
+                                               const uint8_t* __restrict__ qb,
+                                               const uint16_t* __restrict__ sb,
+                                               size_t rowbytes, int nb, const int (&rowidx)[RW],
+                                               const float* xs, int kb0, int kb1, int lane,
+                                               float (&ta)[RW], float (&tb)[RW]) {
+  constexpr int QB = QTraits<QT>::QB;
+  for (int b = kb0 + lane; b < kb1; b += 32) {
+    Blk<QT> bqa[RW], bqb[RW];
+    uint16_t bsa[RW], bsb[RW];
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+      bqa[r].load(qa + (size_t)rowidx[r] * rowbytes + (size_t)b * QB);
+      bsa[r] = ld_u16(sa + (size_t)rowidx[r] * nb + b);
+      if (DUAL) {
+        bqb[r].load(qb + (size_t)rowidx[r] * rowbytes + (size_t)b * QB);
+        bsb[r] = ld_u16(sb + (size_t)rowidx[r] * nb + b);
+      }
+    }
+    float2 xr[16];
+    load_x16(xs + (b - kb0) * QK, xr);
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+      ta[r] = fmaf(h2f(bsa[r]), blk_dot(bqa[r], xr), ta[r]);
+      if (DUAL) tb[r] = fmaf(h2f(bsb[r]), blk_dot(bqb[r], xr), tb[r]);
+    }
+  }
+}
+
+}  // namespace qg

@@ -1,0 +1,62 @@
+// qg_internal.h -- launchers shared between the translation units of libqgemm.
+// Host-side only; every launcher enqueues on the given stream and returns the
+// CUDA error of the launch (cudaSuccess when nothing went wrong).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "qgemm.h"
+
+namespace qg {
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// Count one kernel launch (see qg_kernel_launches).
+void note_launch(int n = 1);
+
+// CUDA-core GEMV, 1..8 columns per launch: y = y0 + W x.
+cudaError_t cc_gemv(int qt, const void* q, const uint16_t* scl, int rows, int k,
+                    const uint16_t* x, int ncols, const float* y0, float* y, cudaStream_t s);
+
+// CUDA-core fused gate/up, 1..8 columns per launch: h = f16(SiLU(Wg x) * (Wu x)).
+cudaError_t cc_gate_up_silu(int qt, const void* qg, const uint16_t* sg, const void* qu,
+                            const uint16_t* su, int rows, int k, const uint16_t* x,
+                            int ncols, uint16_t* h, cudaStream_t s);
+
+// Tensor-core (mma.sync) skinny GEMM, 1..16 columns: y = y0 + W x, or, with
+// qu != nullptr, h = f16(SiLU(W x) * (Wu x)). Only for shapes where
+// tc_supported() holds (k % 256 == 0 and a shared-memory plan exists).
+cudaError_t tc_gemm(int qt, const void* q, const uint16_t* scl, const void* qu,
+                    const uint16_t* su, int rows, int k, const uint16_t* x, int ncols,
+                    const float* y0, float* y, uint16_t* h, cudaStream_t s);
+bool tc_supported(int qt, int ncols, bool dual, int rows, int k);
+
+struct MoeArgs {
+  int qt;
+  const void *qg, *qu, *qd;
+  const uint16_t *sg, *su, *sd;
+  int n_expert, ffn, hidden;
+  const int32_t* ids;
+  const float* rw;
+  int topk;
+  bool has_shared;
+  const void *sqg, *squ, *sqd;
+  const uint16_t *ssg, *ssu, *ssd;
+  const uint16_t* x;
+  int ncols;
+  const float* y0;
+  float* y;
+  void* ws;
+  int32_t* err_flag;
+  int32_t* uniq_out;
+};
+size_t moe_ws_bytes(int n_expert, int ffn, int hidden, int ncols, int topk);
+bool moe_shape_supported(int ffn, int hidden, int ncols);
+cudaError_t moe_forward(const MoeArgs& a, cudaStream_t s);
+
+cudaError_t repack_launch(int qt, const void* gguf, int rows, int k, void* q_out,
+                          uint16_t* scl_out, cudaStream_t s);
+
+}  // namespace qg

@@ -1,0 +1,176 @@
+/*
+ * qgemm.h -- C ABI of libqgemm: block-quantised (GGUF Q4_0 / Q8_0) matrix-vector
+ * and skinny matrix-matrix products on one NVIDIA GB300 (sm_103a).
+ *
+ * Formats ("Engine and kernels", pooled.run, section "What it runs"): a block
+ * is 32 weights plus one f16 scale d. Q4_0 stores 4-bit quants q, weight
+ * (q - 8) * d; byte j of a block holds element j in its low nibble and element
+ * j + 16 in its high nibble. Q8_0 stores int8 q, weight q * d.
+ *
+ * Layout ("Architecture", pooled.run, section "Memory and caching": matrices are
+ * repacked at load time into separate nibble and scale arrays so that kernels
+ * read contiguous stripes). A matrix W of `rows` x `k` weights (k a multiple of
+ * 32) is passed as two row-major device arrays:
+ *   quants: Q4_0 uint8 [rows][k/2]  (16 bytes per block, in-block order as GGUF)
+ *           Q8_0 int8  [rows][k]
+ *   scales: uint16 [rows][k/32]      (f16 bit patterns)
+ * Activations X are f16 [ncols][k] (column c is the c-th input vector), outputs
+ * Y are f32 [ncols][rows].
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless stated; the caller owns all memory.
+ *    No entry point allocates device memory.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *    and the call returns without synchronising.
+ *  - Argument errors (NULL, shape, alignment, type, workspace) are detected on
+ *    the host before anything is launched and returned synchronously; nothing
+ *    is written. A launch failure returns QG_ERR_CUDA.
+ *  - Alignment: quant and scale arrays and X must be 16-byte aligned; Y, y0
+ *    4-byte aligned; H 2-byte aligned.
+ *  - Residual: y0 may be NULL (no residual) or point to f32 [ncols][rows];
+ *    y0 == y is allowed (in-place y += W x). Any other overlap of y0 and y is
+ *    QG_ERR_ALIAS.
+ *  - rows == 0 is a valid empty problem: QG_OK, nothing launched.
+ *  - Results are deterministic: the reduction order depends only on the
+ *    problem shape, never on timing or on the number of SMs.
+ *  - Arithmetic: weights are dequantised exactly (every Q4_0/Q8_0 weight is
+ *    exact in f32 as an integer times its scale) and accumulated in f32; no
+ *    partial sum is ever held in f16.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *cudaStream_t;
+
+typedef enum {
+  QG_OK = 0,
+  QG_ERR_NULL = 1,      /* a required pointer is NULL */
+  QG_ERR_SHAPE = 2,     /* k <= 0 or k % 32, rows < 0, ncols/topk/n_expert out of range */
+  QG_ERR_ALIGN = 3,     /* a pointer violates the alignment rule above */
+  QG_ERR_TYPE = 4,      /* unknown quant type */
+  QG_ERR_WORKSPACE = 5, /* workspace NULL or smaller than qmoe_workspace_bytes() */
+  QG_ERR_CUDA = 6,      /* a CUDA runtime error (launch failure, no device, ...) */
+  QG_ERR_ALIAS = 7      /* y0 partially overlaps y */
+} qg_status;
+
+typedef enum { QG_Q4_0 = 2, QG_Q8_0 = 8 } qg_type; /* GGUF type ids */
+
+/* Static, NUL-terminated description of a status code. */
+const char *qg_status_str(qg_status s);
+
+/* ---------------------------------------------------------------------------
+ * Decode GEMV and its batched twins: Y[c] = y0[c] + W X[c], c < ncols, 1 <= ncols <= 8.
+ * ("Engine and kernels", section "Kernel families": cooperative GEMV for decode,
+ * batched GEMV twins for speculative verify; section "Fewer passes": y += W x.)
+ *   nib / qs : quants of W (see layout), scl: scales, rows x k
+ *   x        : f16 [ncols][k]
+ *   y0       : NULL or f32 [ncols][rows] (may equal y)
+ *   y        : f32 [ncols][rows], written
+ * ------------------------------------------------------------------------- */
+qg_status qgemv_q4_0(const uint8_t *nib, const uint16_t *scl, int rows, int k,
+                     const uint16_t *x, int ncols, const float *y0, float *y,
+                     cudaStream_t stream);
+qg_status qgemv_q8_0(const int8_t *qs, const uint16_t *scl, int rows, int k,
+                     const uint16_t *x, int ncols, const float *y0, float *y,
+                     cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Prefill GEMM: Y[c] = y0[c] + W X[c] for 1 <= ncols <= 16, reading each weight
+ * block once for all columns ("Engine and kernels", section "Kernel families",
+ * prefill GEMM; section "Batching and prefill", row-stationary GEMM at 16
+ * columns with split-K pinned per shape). Arguments as qgemv_*, `t` selects the
+ * quant type of `q`.
+ * ------------------------------------------------------------------------- */
+qg_status qgemm_cols(qg_type t, const void *q, const uint16_t *scl, int rows, int k,
+                     const uint16_t *x, int ncols, const float *y0, float *y,
+                     cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Fused FFN gate/up: one sweep over both projections, SiLU(gate) * up applied
+ * before the write ("Engine and kernels", section "Kernel families", fused
+ * gate/up):  H[c][r] = f16( SiLU(g) * u ),  g = (Wg X[c])[r], u = (Wu X[c])[r],
+ * SiLU(z) = z / (1 + e^-z), g and u accumulated in f32.
+ *   qg/sg, qu/su : gate and up matrices, both rows x k, same type t
+ *   x            : f16 [ncols][k], 1 <= ncols <= 16
+ *   h            : f16 [ncols][rows], written
+ * ------------------------------------------------------------------------- */
+qg_status qffn_gate_up_silu(qg_type t, const void *qg, const uint16_t *sg, const void *qu,
+                            const uint16_t *su, int rows, int k, const uint16_t *x,
+                            int ncols, uint16_t *h, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Stacked-expert MoE layer ("Engine and kernels", sections "What it runs" and
+ * "Kernel families": 256 experts, 8 active per token, plus a shared expert;
+ * routing needs no readback. "A 235B model in a browser window", section
+ * "A mixture of experts is a different animal": gate, up and down matrices of
+ * all experts stacked by role; only the routed experts' slices are read).
+ *
+ *   gate/up stacks : [n_expert][ffn][hidden] (quants qg/qu, scales sg/su)
+ *   down stack     : [n_expert][hidden][ffn] (quants qd, scales sd)
+ *   ids            : device int32 [ncols][topk] expert ids (1 <= topk <= 16)
+ *   rw             : device f32   [ncols][topk] routing weights
+ *   shared         : HOST pointer to a qg_expert of device pointers (one more
+ *                    expert of the same shape, added with weight 1), or NULL
+ *   x              : f16 [ncols][hidden], 1 <= ncols <= 8
+ *   y              : f32 [ncols][hidden] =
+ *                    y0 + sum_j rw[c][j] * D_e (SiLU(G_e x_c) * (U_e x_c)) + shared,
+ *                    e = ids[c][j]; the intermediate h is rounded to f16.
+ *   ws, ws_bytes   : device workspace of at least qmoe_workspace_bytes(...) bytes,
+ *                    16-byte aligned; its contents on entry are ignored
+ *   err_flag       : device int32 or NULL. An id outside [0, n_expert) makes that
+ *                    slot contribute 0 and ORs QG_MOE_BAD_ID into *err_flag. The
+ *                    library never clears the flag: zero it before the call and
+ *                    read it after synchronising. No trap, no abort.
+ *   uniq_ids_out   : device int32 [ncols*topk] or NULL: the distinct valid ids in
+ *                    ascending order (each expert slice is read once for all
+ *                    columns that route to it), padded with -1.
+ * ------------------------------------------------------------------------- */
+typedef struct qg_expert {
+  const void *qg;
+  const uint16_t *sg;
+  const void *qu;
+  const uint16_t *su;
+  const void *qd;
+  const uint16_t *sd;
+} qg_expert;
+
+#define QG_MOE_BAD_ID 1
+
+size_t qmoe_workspace_bytes(int n_expert, int ffn, int hidden, int ncols, int topk);
+
+qg_status qmoe_experts(qg_type t, const void *qg, const uint16_t *sg, const void *qu,
+                       const uint16_t *su, const void *qd, const uint16_t *sd,
+                       int n_expert, int ffn, int hidden, const int32_t *ids,
+                       const float *rw, int topk, const qg_expert *shared,
+                       const uint16_t *x, int ncols, const float *y0, float *y,
+                       void *ws, size_t ws_bytes, int32_t *err_flag,
+                       int32_t *uniq_ids_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Load-time repack ("Architecture", section "Memory and caching"): GGUF
+ * interleaved blocks (per block: f16 d, little endian, then 16 (Q4_0) or 32
+ * (Q8_0) quant bytes), rows x k/32 blocks, into the quant and scale arrays of
+ * the layout above. gguf must be 2-byte aligned; q_out and scl_out follow the
+ * layout's alignment rule.
+ * ------------------------------------------------------------------------- */
+qg_status qrepack(qg_type t, const void *gguf, int rows, int k, void *q_out,
+                  uint16_t *scl_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics: number of kernels this library has launched in this process
+ * (monotonic, all devices and threads). Lets a caller count the GPU launches of
+ * a region of work. Not part of the method.
+ * ------------------------------------------------------------------------- */
+uint64_t qg_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QGEMM_H */

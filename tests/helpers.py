@@ -1,0 +1,46 @@
+"""Shared helpers of the GPU parity tests: device upload, tolerance checks."""
+import os
+
+import numpy as np
+
+NTHREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def dev(a, dtype=None):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def dev_u16_as_f16(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.float16)
+
+
+def dev_u16(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def assert_within(got, ref, bound, what=""):
+    """|got - ref| <= bound elementwise (all f64), with a readable failure."""
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        i = tuple(int(v) for v in i)
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; first {i}: "
+            f"got {got[i]!r} ref {ref[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
+
+
+def gemv_bound(S):
+    """The product tolerance: |y_gpu - y_ref| <= 1e-3 * sum_k |w_k||x_k| + 1e-6."""
+    return 1e-3 * S + 1e-6

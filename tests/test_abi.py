@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function declared in include/qgemm.h, and rejects bad arguments with the
+documented status codes before launching anything."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import gemm_q4_q8_gb300 as qg
+from gemm_q4_q8_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qg.load()
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    names = re.findall(r"\b(q[a-z0-9_]+)\s*\(", txt)
+    return sorted(set(n for n in names if not n.startswith("qg_expert")))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in qg.EXPORTS:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.qg_status_str(code).decode()
+        assert s and s != "unknown status"
+    assert lib.qg_status_str(99).decode() == "unknown status"
+
+
+ALIGNED = 0x10000  # a fake, 16-byte aligned address; never dereferenced
+
+
+def gemv(lib, **kw):
+    a = dict(q=ALIGNED, scl=ALIGNED, rows=64, k=64, x=ALIGNED, ncols=1, y0=None, y=ALIGNED + 0x100000)
+    a.update(kw)
+    return lib.qgemv_q4_0(a["q"], a["scl"], a["rows"], a["k"], a["x"], a["ncols"], a["y0"], a["y"], None)
+
+
+def test_shape_errors(lib):
+    assert gemv(lib, k=48) == 2
+    assert gemv(lib, k=0) == 2
+    assert gemv(lib, k=-32) == 2
+    assert gemv(lib, rows=-1) == 2
+    assert gemv(lib, ncols=0) == 2
+    assert gemv(lib, ncols=9) == 2
+    assert lib.qgemm_cols(2, ALIGNED, ALIGNED, 64, 64, ALIGNED, 17, None, ALIGNED, None) == 2
+    assert lib.qffn_gate_up_silu(2, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 64, 64, ALIGNED, 17, ALIGNED, None) == 2
+
+
+def test_type_errors(lib):
+    assert lib.qgemm_cols(3, ALIGNED, ALIGNED, 64, 64, ALIGNED, 1, None, ALIGNED, None) == 4
+    assert lib.qrepack(7, ALIGNED, 4, 64, ALIGNED, ALIGNED, None) == 4
+
+
+def test_null_errors(lib):
+    assert gemv(lib, q=None) == 1
+    assert gemv(lib, scl=None) == 1
+    assert gemv(lib, x=None) == 1
+    assert gemv(lib, y=None) == 1
+    assert lib.qffn_gate_up_silu(2, ALIGNED, ALIGNED, None, ALIGNED, 64, 64, ALIGNED, 2, ALIGNED, None) == 1
+
+
+def test_align_errors(lib):
+    assert gemv(lib, q=ALIGNED + 8) == 3
+    assert gemv(lib, scl=ALIGNED + 2) == 3
+    assert gemv(lib, x=ALIGNED + 4) == 3
+    assert gemv(lib, y=ALIGNED + 0x100002) == 3
+    assert gemv(lib, y0=ALIGNED + 0x200001) == 3
+
+
+def test_alias_error(lib):
+    # y0 overlapping y without being equal to it
+    assert gemv(lib, y0=ALIGNED + 0x100000 + 16) == 7
+
+
+def test_empty_problem_is_ok(lib):
+    assert gemv(lib, rows=0, q=None, scl=None, x=None, y=None) == 0
+    assert lib.qrepack(2, None, 0, 64, None, None, None) == 0
+
+
+def test_moe_argument_errors(lib):
+    w = lib.qmoe_workspace_bytes(256, 512, 2048, 8, 8)
+    assert w > 0
+    assert lib.qmoe_workspace_bytes(256, 512, 2048, 9, 8) == 0
+
+    def moe(**kw):
+        a = dict(t=8, n_expert=4, ffn=64, hidden=64, topk=2, ncols=2, ws=ALIGNED, wsb=1 << 30,
+                 ids=ALIGNED, y=ALIGNED)
+        a.update(kw)
+        return lib.qmoe_experts(a["t"], ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED,
+                                a["n_expert"], a["ffn"], a["hidden"], a["ids"], ALIGNED, a["topk"],
+                                None, ALIGNED, a["ncols"], None, a["y"], a["ws"], a["wsb"], None,
+                                None, None)
+    assert moe(t=5) == 4
+    assert moe(ncols=9) == 2
+    assert moe(topk=0) == 2
+    assert moe(topk=17) == 2
+    assert moe(n_expert=0) == 2
+    assert moe(ffn=48) == 2
+    assert moe(ids=None) == 1
+    assert moe(wsb=16) == 5
+    assert moe(ws=None) == 5
+    assert moe(ids=ALIGNED + 2) == 3
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    from conftest import gpu_available
+    if gpu_available():
+        pytest.skip("a GPU is present")
+    # valid arguments: the library must fail loudly (no CPU fallback)
+    assert gemv(lib) == 6
