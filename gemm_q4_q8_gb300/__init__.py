@@ -19,7 +19,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqgemm.so")
 
 EXPORTS = ("qg_status_str", "qgemv_q4_0", "qgemv_q8_0", "qgemm_cols", "qffn_gate_up_silu",
-           "qmoe_workspace_bytes", "qmoe_experts", "qrepack", "qg_kernel_launches")
+           "qmoe_workspace_bytes", "qmoe_experts", "qmoe_experts_noalloc", "qrepack",
+           "qg_kernel_launches")
+
+QG_MOE_NOALLOC_WS_BYTES = 8 << 20
 
 STATUS = {0: "QG_OK", 1: "QG_ERR_NULL", 2: "QG_ERR_SHAPE", 3: "QG_ERR_ALIGN", 4: "QG_ERR_TYPE",
           5: "QG_ERR_WORKSPACE", 6: "QG_ERR_CUDA", 7: "QG_ERR_ALIAS"}
@@ -60,6 +63,8 @@ def load(path: str | None = None):
     L.qmoe_workspace_bytes.restype = sz
     L.qmoe_experts.argtypes = [i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32,
                                C.POINTER(QGExpert), vp, i32, vp, vp, vp, sz, vp, vp, vp]
+    L.qmoe_experts_noalloc.argtypes = [i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32,
+                                       C.POINTER(QGExpert), vp, i32, vp, vp, vp, vp, vp]
     L.qrepack.argtypes = [i32, vp, i32, i32, vp, vp, vp]
     L.qg_kernel_launches.argtypes = []
     L.qg_kernel_launches.restype = C.c_uint64
@@ -134,6 +139,21 @@ def qmoe_experts(qtype, qg, sg, qu, su, qd, sd, n_expert, ffn, hidden, ids, rw, 
                                _ptr(x), ncols, _ptr(y0), _ptr(y), _ptr(ws),
                                ws.numel() * ws.element_size(), _ptr(err_flag),
                                _ptr(uniq_ids_out), _stream(stream)))
+
+
+def qmoe_experts_noalloc(qtype, qg, sg, qu, su, qd, sd, n_expert, ffn, hidden, ids, rw, x, y,
+                         y0=None, shared=None, err_flag=None, uniq_ids_out=None, stream=None):
+    """qmoe_experts with the library's built-in workspace (no caller allocation);
+    problems needing more than QG_MOE_NOALLOC_WS_BYTES raise QG_ERR_WORKSPACE."""
+    sh = None
+    if shared is not None:
+        sh = C.pointer(QGExpert(*[_ptr(shared[n]) for n in ("qg", "sg", "qu", "su", "qd", "sd")]))
+    ncols, topk = ids.shape
+    _check("qmoe_experts_noalloc",
+           load().qmoe_experts_noalloc(int(qtype), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su),
+                                       _ptr(qd), _ptr(sd), n_expert, ffn, hidden, _ptr(ids),
+                                       _ptr(rw), topk, sh, _ptr(x), ncols, _ptr(y0), _ptr(y),
+                                       _ptr(err_flag), _ptr(uniq_ids_out), _stream(stream)))
 
 
 def qg_kernel_launches() -> int:

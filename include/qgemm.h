@@ -154,6 +154,31 @@ qg_status qmoe_experts(qg_type t, const void *qg, const uint16_t *sg, const void
                        int32_t *uniq_ids_out, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * qmoe_experts without a caller workspace. The pages have no counterpart to
+ * this call: it exists for callers that cannot allocate device memory (a
+ * plugin inside a framework that owns all device memory, a fixed memory budget
+ * with no room left, a latency-critical loop that must not call cudaMalloc).
+ * Arguments and results are those of qmoe_experts minus ws / ws_bytes; the
+ * workspace is a QG_MOE_NOALLOC_WS_BYTES array inside the library, held on every
+ * GPU that loads the library until the process exits.
+ *  - Problems whose qmoe_workspace_bytes(...) exceeds QG_MOE_NOALLOC_WS_BYTES
+ *    return QG_ERR_WORKSPACE before anything is launched.
+ *  - The first call on each device (with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - All calls share the array: calls whose GPU work overlaps (different
+ *    streams, several host threads) race on it. Nothing in it needs clearing.
+ *  - Allocates nothing (no cudaMalloc, no library allocator).
+ * ------------------------------------------------------------------------- */
+#define QG_MOE_NOALLOC_WS_BYTES ((size_t)8 << 20) /* 8 MiB */
+
+qg_status qmoe_experts_noalloc(qg_type t, const void *qg, const uint16_t *sg, const void *qu,
+                               const uint16_t *su, const void *qd, const uint16_t *sd,
+                               int n_expert, int ffn, int hidden, const int32_t *ids,
+                               const float *rw, int topk, const qg_expert *shared,
+                               const uint16_t *x, int ncols, const float *y0, float *y,
+                               int32_t *err_flag, int32_t *uniq_ids_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Load-time repack ("Architecture", section "Memory and caching"): GGUF
  * interleaved blocks (per block: f16 d, little endian, then 16 (Q4_0) or 32
  * (Q8_0) quant bytes), rows x k/32 blocks, into the quant and scale arrays of

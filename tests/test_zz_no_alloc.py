@@ -1,0 +1,78 @@
+"""qmoe_experts_noalloc: the MoE layer for callers that cannot allocate device
+memory (the workspace is an array inside the library). Checked through the C
+ABI against qmoe_experts with a caller-allocated workspace, on two calls in a
+row, within the MoE tolerance the other tests use (the oracle's propagated
+bound). This file is collected last so that a failure here stops a run only
+after every other test has run."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import assert_within, dev, dev_u16, dev_u16_as_f16, host
+
+torch = pytest.importorskip("torch")
+
+import gemm_q4_q8_gb300 as qg  # noqa: E402
+
+
+def _moe_args(case):
+    sh = None
+    if case.get("shared") is not None:
+        sh = {n: (dev_u16(v) if n.startswith("s") else dev(v)) for n, v in case["shared"].items()}
+    y0 = dev(case["y0"]) if case.get("y0") is not None else None
+    return dict(qg=dev(case["qg"]), sg=dev_u16(case["sg"]), qu=dev(case["qu"]),
+                su=dev_u16(case["su"]), qd=dev(case["qd"]), sd=dev_u16(case["sd"]),
+                ids=dev(np.ascontiguousarray(case["ids"], np.int32)), rw=dev(case["rw"]),
+                x=dev_u16_as_f16(case["x"]), y0=y0, shared=sh)
+
+
+def _run(case, a, noalloc):
+    ncols, hidden = case["ncols"], case["hidden"]
+    y = torch.full((ncols, hidden), float("nan"), dtype=torch.float32, device="cuda")
+    uniq = torch.full((ncols * case["topk"],), -9, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    common = (case["qtype"], a["qg"], a["sg"], a["qu"], a["su"], a["qd"], a["sd"],
+              case["n_expert"], case["ffn"], hidden, a["ids"], a["rw"], a["x"], y)
+    if noalloc:
+        qg.qmoe_experts_noalloc(*common, y0=a["y0"], shared=a["shared"], err_flag=err,
+                                uniq_ids_out=uniq)
+    else:
+        nb = qg.qmoe_workspace_bytes(case["n_expert"], case["ffn"], hidden, ncols, case["topk"])
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        qg.qmoe_experts(*common, ws, y0=a["y0"], shared=a["shared"], err_flag=err,
+                        uniq_ids_out=uniq)
+    torch.cuda.synchronize()
+    return host(y), host(uniq), int(host(err)[0])
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gemm_q4_q8_gb300 import build
+    build.build()
+    oracle.build()
+    cases = [synth.moe_layer(8, seed=11),
+             synth.moe_case(synth.Q4_0, 16, 64, 256, 5, topk=3, shared=True, residual=True,
+                            seed=12)]
+    for case in cases:  # two noalloc calls in a row, the second on different data
+        a = _moe_args(case)
+        y_ws, u_ws, e_ws = _run(case, a, noalloc=False)
+        y_na, u_na, e_na = _run(case, a, noalloc=True)
+        _, bound, _, _, _ = oracle.moe(case)
+        assert np.isfinite(y_na).all()
+        assert_within(y_na, y_ws.astype(np.float64), bound, "noalloc vs caller workspace")
+        assert np.array_equal(u_na, u_ws) and e_na == e_ws == 0
+
+
+def test_noalloc_rejects_problems_beyond_its_workspace():
+    from gemm_q4_q8_gb300 import build
+    build.build()
+    L = qg.load()
+    # 16 columns is out of range for any MoE call; a large layer exceeds 8 MiB
+    assert qg.qmoe_workspace_bytes(256, 4096, 8192, 8, 16) > qg.QG_MOE_NOALLOC_WS_BYTES
+    st = L.qmoe_experts_noalloc(8, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 256,
+                                4096, 8192, 0x10000, 0x10000, 16, None, 0x10000, 8, None,
+                                0x10000, None, None, None)
+    assert st == 5  # QG_ERR_WORKSPACE, nothing launched
