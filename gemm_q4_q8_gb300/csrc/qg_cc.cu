@@ -25,9 +25,17 @@ constexpr int CC_WARPS = 8;
 constexpr int CC_THREADS = CC_WARPS * 32;
 constexpr int CC_XSMEM_FLOATS = 24576;  // 96 KB of staged x per CTA
 
-template <int NC> struct CCShape {
-  static constexpr int RW = NC >= 8 ? 1 : (NC >= 4 ? 2 : (NC >= 2 ? 4 : 8));
+// Rows per warp: 8 for one column (x reused across 8 rows), fewer for more
+// columns (at most 16 accumulators per thread), and fewer again when a matrix
+// is too small to give every SM work. The row count never changes a result:
+// each row is summed by one warp, blocks in order per lane, then the same
+// lane butterfly.
+template <int NC, int RW_> struct CCShape {
+  static constexpr int RW = RW_;
   static constexpr int V = RW * NC <= 1 ? 1 : (RW * NC <= 2 ? 2 : (RW * NC <= 4 ? 4 : (RW * NC <= 8 ? 8 : (RW * NC <= 16 ? 16 : 32))));
+};
+template <int NC> struct CCDefaultRW {
+  static constexpr int RW = NC >= 8 ? 1 : (NC >= 4 ? 2 : (NC >= 2 ? 4 : 8));
 };
 
 struct CCParams {
@@ -46,10 +54,10 @@ struct CCParams {
 
 enum { EPI_F32 = 0, EPI_SILU = 1 };
 
-template <int QT, int NC, bool DUAL, int EPI>
-__global__ void __launch_bounds__(CC_THREADS)
+template <int QT, int NC, int RW_, bool DUAL, int EPI>
+__global__ void __launch_bounds__(CC_THREADS, NC == 1 ? 2 : 1)
 qmv_cc_kernel(const CCParams p) {
-  using S = CCShape<NC>;
+  using S = CCShape<NC, RW_>;
   constexpr int RW = S::RW;
   constexpr int V = S::V;
   constexpr int QB = QTraits<QT>::QB;
@@ -177,7 +185,7 @@ qmv_cc_kernel(const CCParams p) {
 }
 
 // ------------------------------------------------------------- launchers
-template <int QT, int NC, bool DUAL, int EPI>
+template <int QT, int NC, int RW, bool DUAL, int EPI>
 static cudaError_t launch_cc_t(const CCParams& p0, cudaStream_t s, int* nlaunch) {
   CCParams p = p0;
   const int nb = p.k / QK;
@@ -185,7 +193,7 @@ static cudaError_t launch_cc_t(const CCParams& p0, cudaStream_t s, int* nlaunch)
   if (cb > nb) cb = nb;
   p.cb = cb;
   const size_t smem = (size_t)NC * cb * QK * sizeof(float);
-  auto kern = qmv_cc_kernel<QT, NC, DUAL, EPI>;
+  auto kern = qmv_cc_kernel<QT, NC, RW, DUAL, EPI>;
   static int occ = -1;
   static size_t occ_smem = 0;
   if (occ < 0 || occ_smem != smem) {
@@ -196,7 +204,6 @@ static cudaError_t launch_cc_t(const CCParams& p0, cudaStream_t s, int* nlaunch)
     if (occ < 1) occ = 1;
     occ_smem = smem;
   }
-  constexpr int RW = CCShape<NC>::RW;
   const long ngroups = (p.rows + RW - 1) / RW;
   long grid = (ngroups + CC_WARPS - 1) / CC_WARPS;
   const long maxgrid = (long)device_sm_count() * occ;
@@ -211,14 +218,19 @@ static cudaError_t launch_cc_t(const CCParams& p0, cudaStream_t s, int* nlaunch)
 template <int QT, bool DUAL, int EPI>
 static cudaError_t dispatch_nc(int nc, const CCParams& p, cudaStream_t s, int* nl) {
   switch (nc) {
-    case 1: return launch_cc_t<QT, 1, DUAL, EPI>(p, s, nl);
-    case 2: return launch_cc_t<QT, 2, DUAL, EPI>(p, s, nl);
-    case 3: return launch_cc_t<QT, 3, DUAL, EPI>(p, s, nl);
-    case 4: return launch_cc_t<QT, 4, DUAL, EPI>(p, s, nl);
-    case 5: return launch_cc_t<QT, 5, DUAL, EPI>(p, s, nl);
-    case 6: return launch_cc_t<QT, 6, DUAL, EPI>(p, s, nl);
-    case 7: return launch_cc_t<QT, 7, DUAL, EPI>(p, s, nl);
-    case 8: return launch_cc_t<QT, 8, DUAL, EPI>(p, s, nl);
+    case 1: {
+      // 8 rows per warp unless that leaves SMs idle (fewer than 2 CTAs per SM)
+      const long ctas8 = ((long)p.rows + 8 * CC_WARPS - 1) / (8 * CC_WARPS);
+      if (ctas8 >= 2L * device_sm_count()) return launch_cc_t<QT, 1, 8, DUAL, EPI>(p, s, nl);
+      return launch_cc_t<QT, 1, 2, DUAL, EPI>(p, s, nl);
+    }
+    case 2: return launch_cc_t<QT, 2, CCDefaultRW<2>::RW, DUAL, EPI>(p, s, nl);
+    case 3: return launch_cc_t<QT, 3, CCDefaultRW<3>::RW, DUAL, EPI>(p, s, nl);
+    case 4: return launch_cc_t<QT, 4, CCDefaultRW<4>::RW, DUAL, EPI>(p, s, nl);
+    case 5: return launch_cc_t<QT, 5, CCDefaultRW<5>::RW, DUAL, EPI>(p, s, nl);
+    case 6: return launch_cc_t<QT, 6, CCDefaultRW<6>::RW, DUAL, EPI>(p, s, nl);
+    case 7: return launch_cc_t<QT, 7, CCDefaultRW<7>::RW, DUAL, EPI>(p, s, nl);
+    case 8: return launch_cc_t<QT, 8, CCDefaultRW<8>::RW, DUAL, EPI>(p, s, nl);
   }
   return cudaErrorInvalidValue;
 }

@@ -85,27 +85,36 @@ __device__ __forceinline__ void load_x16(const float* p, float2 (&xr)[16]) {
 }
 
 // Stage x[c][kb0*32 .. kb1*32) of the selected columns into shared memory as
-// f32 in the consumption order of QT.
+// f32 in the consumption order of QT. One thread per 32-element block: its four
+// 16-byte loads are issued before any use, so a CTA pays about one global-load
+// latency per pass instead of one per element.
+__device__ __forceinline__ void stage_block(int qt, float* dst, const __half* src) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  const uint4 v0 = s4[0], v1 = s4[1], v2 = s4[2], v3 = s4[3];
+  __align__(16) __half h[32];
+  *reinterpret_cast<uint4*>(&h[0]) = v0;
+  *reinterpret_cast<uint4*>(&h[8]) = v1;
+  *reinterpret_cast<uint4*>(&h[16]) = v2;
+  *reinterpret_cast<uint4*>(&h[24]) = v3;
+  float o[32];
+#pragma unroll
+  for (int s = 0; s < 32; ++s)
+    o[s] = qt == T_Q4_0 ? __half2float(h[q4_xorder_elem(s)]) * q4_xorder_scale(s)
+                        : __half2float(h[s]);
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+}
+
 template <int QT, int NC>
 __device__ __forceinline__ void stage_x(float* xs, int xstride, const __half* x, int k,
                                         const int (&cols)[NC], int kb0, int kb1) {
-  const int n = (kb1 - kb0) * QK;
-  for (int c = 0; c < NC; ++c) {
-    const __half* xc = x + (size_t)cols[c] * k + (size_t)kb0 * QK;
-    float* dst = xs + c * xstride;
-    for (int s = threadIdx.x; s < n; s += blockDim.x) {
-      const int b = s >> 5, j = s & 31;
-      float v;
-      if (QT == T_Q4_0) {
-        v = __half2float(xc[b * QK + q4_xorder_elem(j)]) * q4_xorder_scale(j);
-      } else {
-        v = __half2float(xc[s]);
-      }
-      dst[s] = v;
-    }
+  const int nbk = kb1 - kb0;
+  for (int it = threadIdx.x; it < NC * nbk; it += blockDim.x) {
+    const int c = it / nbk, b = it % nbk;
+    stage_block(QT, xs + c * xstride + b * QK, x + (size_t)cols[c] * k + (size_t)(kb0 + b) * QK);
   }
 }
-
 
 // One warp: 1-column dot of RW rows (and of a second matrix when DUAL) over
 // the blocks [kb0, kb1) of the staged x chunk; lane l takes blocks kb0+l,

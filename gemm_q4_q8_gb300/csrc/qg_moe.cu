@@ -101,20 +101,16 @@ __device__ void moe_route(const MoeDev& p, MoeRoute& R) {
   __syncthreads();
 }
 
+// Stage the selected columns of x (column stride `colstride` halves, k wide)
+// as f32 in the consumption order of qt, one 32-element block per thread.
 __device__ __forceinline__ void stage_x_rt(int qt, float* xs, int xstride, const __half* x,
                                            size_t colstride, uint32_t cmask, int ncols,
                                            int k) {
-  const int n = k;
-  for (int c = 0; c < ncols; ++c) {
+  const int nbk = k / QK;
+  for (int it = threadIdx.x; it < ncols * nbk; it += blockDim.x) {
+    const int c = it / nbk, b = it % nbk;
     if (!((cmask >> c) & 1u)) continue;
-    const __half* xc = x + (size_t)c * colstride;
-    float* dst = xs + c * xstride;
-    for (int s = threadIdx.x; s < n; s += blockDim.x) {
-      const int b = s >> 5, j = s & 31;
-      dst[s] = (qt == T_Q4_0)
-                   ? __half2float(xc[b * QK + q4_xorder_elem(j)]) * q4_xorder_scale(j)
-                   : __half2float(xc[s]);
-    }
+    stage_block(qt, xs + c * xstride + b * QK, x + (size_t)c * colstride + (size_t)b * QK);
   }
 }
 

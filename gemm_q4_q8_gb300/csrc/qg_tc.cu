@@ -251,32 +251,42 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 
   // Permute x for this CTA's K range: for block b, column c, lane slot t, the
   // 16 bytes [x4t, x4t+2, x4t+1, x4t+3, x4t+16, x4t+18, x4t+17, x4t+19].
+  // Four items per thread per pass, all sixteen 16-byte loads issued first.
   {
-    const int nblk = nu * 8;
-    const int items = nblk * S::CPAD;
-    for (int it = tid; it < items; it += TC_THREADS) {
-      const int b = it / S::CPAD, c = it % S::CPAD;
-      uint4 out[4];
-      if (c < p.ncols) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)c * p.k +
-                                                          (size_t)(u0 * 8 + b) * QK);
-        const uint4 q0 = src[0], q1 = src[1], q2 = src[2], q3 = src[3];
-        const uint32_t lo[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        const uint32_t hi[8] = {q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+    const int items = nu * 8 * S::CPAD;
+    for (int base = tid; base < items; base += 4 * TC_THREADS) {
+      uint4 q[4][4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          out[t].x = __byte_perm(lo[2 * t], lo[2 * t + 1], 0x5410);
-          out[t].y = __byte_perm(lo[2 * t], lo[2 * t + 1], 0x7632);
-          out[t].z = __byte_perm(hi[2 * t], hi[2 * t + 1], 0x5410);
-          out[t].w = __byte_perm(hi[2 * t], hi[2 * t + 1], 0x7632);
+      for (int u = 0; u < 4; ++u) {
+        const int it = base + u * TC_THREADS;
+        const int b = it / S::CPAD, c = it % S::CPAD;
+        if (it < items && c < p.ncols) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)c * p.k +
+                                                            (size_t)(u0 * 8 + b) * QK);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) q[u][v] = src[v];
+        } else {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) q[u][v] = make_uint4(0, 0, 0, 0);
         }
-      } else {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) out[t] = make_uint4(0, 0, 0, 0);
       }
-      uint4* dst = reinterpret_cast<uint4*>(xperm + ((size_t)(b * S::CPAD + c) * 4) * 16);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) dst[t] = out[t];
+      for (int u = 0; u < 4; ++u) {
+        const int it = base + u * TC_THREADS;
+        if (it >= items) continue;
+        const int b = it / S::CPAD, c = it % S::CPAD;
+        const uint32_t lo[8] = {q[u][0].x, q[u][0].y, q[u][0].z, q[u][0].w,
+                                q[u][1].x, q[u][1].y, q[u][1].z, q[u][1].w};
+        const uint32_t hi[8] = {q[u][2].x, q[u][2].y, q[u][2].z, q[u][2].w,
+                                q[u][3].x, q[u][3].y, q[u][3].z, q[u][3].w};
+        uint4* dst = reinterpret_cast<uint4*>(xperm + ((size_t)(b * S::CPAD + c) * 4) * 16);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          dst[t] = make_uint4(__byte_perm(lo[2 * t], lo[2 * t + 1], 0x5410),
+                              __byte_perm(lo[2 * t], lo[2 * t + 1], 0x7632),
+                              __byte_perm(hi[2 * t], hi[2 * t + 1], 0x5410),
+                              __byte_perm(hi[2 * t], hi[2 * t + 1], 0x7632));
+      }
     }
   }
   __syncthreads();
@@ -313,63 +323,92 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       if (!mbar_wait(&full[s], (uint32_t)((i / ns) & 1))) break;
       const uint32_t st = smem_u32(stages + (size_t)s * S::STAGE);
       const uint32_t sbase = st + S::NMAT * S::A_BYTES;
+      // the 8 f16 scales of rows g and g+8 for this unit, per matrix
+      uint4 sg4[S::NMAT], sg84[S::NMAT];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        // the four blocks (of 8 in the unit) handled by this k-group
-        const int blk = QT == T_Q4_0 ? (2 * kj + 4 * (j >> 1) + (j & 1)) : (kj + 2 * j);
-        uint4 bf[NT];
+      for (int m = 0; m < S::NMAT; ++m) {
+        sg4[m] = lds128(sbase + m * S::S_BYTES + srow_g);
+        sg84[m] = lds128(sbase + m * S::S_BYTES + srow_g8);
+      }
 #pragma unroll
-        for (int n = 0; n < NT; ++n)
-          bf[n] = lds128(xp_base + (uint32_t)((((i * 8 + blk) * S::CPAD + n * 8 + g) * 4 + t) * 16));
+      for (int pr = 0; pr < 2; ++pr) {
+        // Q4_0: blocks (c0, c0+1), c0 = 2kj + 4pr, from one ldmatrix.x4 per matrix.
+        // Q8_0: blocks kj + 4pr and kj + 4pr + 2, one ldmatrix.x4 each.
+        uint32_t W[S::NMAT][2][4];  // [matrix][block of the pair][r0..r3]
 #pragma unroll
         for (int m = 0; m < S::NMAT; ++m) {
           const uint32_t abase = st + m * S::A_BYTES;
-          uint32_t wg, wg8, vg, vg8;  // Q4_0: words of rows g, g+8; Q8_0: both halves
           if (QT == T_Q4_0) {
-            // one ldmatrix.x4 covers the block pair (c0, c0+1); reuse across j
-            const int c0 = 2 * kj + 4 * (j >> 1);
-            const int chunk = c0 + lchunk;
+            const int chunk = 2 * kj + 4 * pr + lchunk;
             uint32_t r0, r1, r2, r3;
             ldsm_x4(abase + (uint32_t)(lrow * 128 + ((chunk ^ (lrow & 7)) << 4)), r0, r1, r2, r3);
-            wg = (j & 1) ? r2 : r0;
-            wg8 = (j & 1) ? r3 : r1;
-            vg = vg8 = 0;
+            W[m][0][0] = r0; W[m][0][1] = r1; W[m][1][0] = r2; W[m][1][1] = r3;
+            W[m][0][2] = W[m][0][3] = W[m][1][2] = W[m][1][3] = 0;
           } else {
-            const int bx = blk >> 2, c0 = 2 * (blk & 3);
-            const int chunk = c0 + lchunk;
-            ldsm_x4(abase + (uint32_t)(bx * TC_BM * 128 + lrow * 128 + ((chunk ^ (lrow & 7)) << 4)),
-                    wg, wg8, vg, vg8);
-          }
-          uint32_t A0[4], A1[4];
-          if (QT == T_Q4_0) {
-            uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
-            dq4_f16(wg, e0, e1, e2, e3);
-            dq4_f16(wg8, f0, f1, f2, f3);
-            A0[0] = e0; A0[1] = f0; A0[2] = e2; A0[3] = f2;
-            A1[0] = e1; A1[1] = f1; A1[2] = e3; A1[3] = f3;
-          } else {
-            uint32_t p0, p1, q0, q1;
-            dq8_f16(wg, p0, p1);
-            dq8_f16(wg8, q0, q1);
-            A0[0] = p0; A0[1] = q0; A0[2] = p1; A0[3] = q1;
-            dq8_f16(vg, p0, p1);
-            dq8_f16(vg8, q0, q1);
-            A1[0] = p0; A1[1] = q0; A1[2] = p1; A1[3] = q1;
-          }
-          const uint32_t sb = sbase + m * S::S_BYTES + (uint32_t)(blk * 2);
-          const float dg = h2f(lds16(sb + srow_g));
-          const float dg8 = h2f(lds16(sb + srow_g8));
 #pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            float fr[4];
-            mma16816(fr, A0, bf[n].x, bf[n].y);
-            mma16816_acc(fr, A1, bf[n].z, bf[n].w);
-            float2 lo = fma2(make_float2(dg, dg), make_float2(fr[0], fr[1]),
-                             make_float2(acc[m][n][0], acc[m][n][1]));
-            float2 hi = fma2(make_float2(dg8, dg8), make_float2(fr[2], fr[3]),
-                             make_float2(acc[m][n][2], acc[m][n][3]));
-            acc[m][n][0] = lo.x; acc[m][n][1] = lo.y;
-            acc[m][n][2] = hi.x; acc[m][n][3] = hi.y;
+            for (int sub = 0; sub < 2; ++sub) {
+              const int blk = kj + 4 * pr + 2 * sub;
+              const int bx = blk >> 2, chunk = 2 * (blk & 3) + lchunk;
+              ldsm_x4(abase + (uint32_t)(bx * TC_BM * 128 + lrow * 128 + ((chunk ^ (lrow & 7)) << 4)),
+                      W[m][sub][0], W[m][sub][1], W[m][sub][2], W[m][sub][3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const int blk = QT == T_Q4_0 ? (2 * kj + 4 * pr + sub) : (kj + 4 * pr + 2 * sub);
+          uint4 bf[NT];
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+            bf[n] = lds128(xp_base + (uint32_t)((((i * 8 + blk) * S::CPAD + n * 8 + g) * 4 + t) * 16));
+#pragma unroll
+          for (int m = 0; m < S::NMAT; ++m) {
+            uint32_t A0[4], A1[4];
+            if (QT == T_Q4_0) {
+              uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
+              dq4_f16(W[m][sub][0], e0, e1, e2, e3);
+              dq4_f16(W[m][sub][1], f0, f1, f2, f3);
+              A0[0] = e0; A0[1] = f0; A0[2] = e2; A0[3] = f2;
+              A1[0] = e1; A1[1] = f1; A1[2] = e3; A1[3] = f3;
+            } else {
+              uint32_t p0, p1, q0, q1;
+              dq8_f16(W[m][sub][0], p0, p1);
+              dq8_f16(W[m][sub][1], q0, q1);
+              A0[0] = p0; A0[1] = q0; A0[2] = p1; A0[3] = q1;
+              dq8_f16(W[m][sub][2], p0, p1);
+              dq8_f16(W[m][sub][3], q0, q1);
+              A1[0] = p0; A1[1] = q0; A1[2] = p1; A1[3] = q1;
+            }
+            // scale of block blk (word blk/2, half blk%2) without indexed registers:
+            // Q4_0: word kj + 2pr, half sub; Q8_0: word 2pr + sub, half kj.
+            uint32_t sw, sw8;
+            bool hi_half;
+            if (QT == T_Q4_0) {
+              const uint32_t a0 = pr ? sg4[m].z : sg4[m].x, a1 = pr ? sg4[m].w : sg4[m].y;
+              const uint32_t b0 = pr ? sg84[m].z : sg84[m].x, b1 = pr ? sg84[m].w : sg84[m].y;
+              sw = kj ? a1 : a0;
+              sw8 = kj ? b1 : b0;
+              hi_half = sub != 0;
+            } else {
+              const int wi = 2 * pr + sub;
+              sw = wi == 0 ? sg4[m].x : (wi == 1 ? sg4[m].y : (wi == 2 ? sg4[m].z : sg4[m].w));
+              sw8 = wi == 0 ? sg84[m].x : (wi == 1 ? sg84[m].y : (wi == 2 ? sg84[m].z : sg84[m].w));
+              hi_half = kj != 0;
+            }
+            const float dg = h2f((uint16_t)(hi_half ? (sw >> 16) : (sw & 0xffffu)));
+            const float dg8 = h2f((uint16_t)(hi_half ? (sw8 >> 16) : (sw8 & 0xffffu)));
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              float fr[4];
+              mma16816(fr, A0, bf[n].x, bf[n].y);
+              mma16816_acc(fr, A1, bf[n].z, bf[n].w);
+              float2 lo = fma2(make_float2(dg, dg), make_float2(fr[0], fr[1]),
+                               make_float2(acc[m][n][0], acc[m][n][1]));
+              float2 hi = fma2(make_float2(dg8, dg8), make_float2(fr[2], fr[3]),
+                               make_float2(acc[m][n][2], acc[m][n][3]));
+              acc[m][n][0] = lo.x; acc[m][n][1] = lo.y;
+              acc[m][n][2] = hi.x; acc[m][n][3] = hi.y;
+            }
           }
         }
       }
