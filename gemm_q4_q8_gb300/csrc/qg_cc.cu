@@ -121,10 +121,9 @@ qmv_cc_kernel(const CCParams p) {
             sb[r] = ld_u16(p.sb + (size_t)rowidx[r] * nb + b);
           }
         }
-        const float* xb = xs + (b - kb0) * QK;
         if (NC == 1) {
           float2 xr[16];
-          load_x16(xb, xr);
+          load_x16(xs, cb, b - kb0, xr);
 #pragma unroll
           for (int r = 0; r < RW; ++r) {
             ta[r][0] = fmaf(h2f(sa[r]), blk_dot(qa[r], xr), ta[r][0]);
@@ -141,7 +140,7 @@ qmv_cc_kernel(const CCParams p) {
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
               float2 xr[16];
-              load_x16(xb + c * xstride, xr);
+              load_x16(xs + c * xstride, cb, b - kb0, xr);
               ta[r][c] = fmaf(da, wv_dot(wa, xr), ta[r][c]);
               if (DUAL) tb[r][c] = fmaf(db, wv_dot(wb, xr), tb[r][c]);
             }

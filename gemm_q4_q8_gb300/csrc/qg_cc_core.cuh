@@ -74,11 +74,15 @@ __device__ __forceinline__ float wv_dot(const float2 (&wv)[16], const float2 (&x
   return (a0.x + a0.y) + (a1.x + a1.y);
 }
 
-__device__ __forceinline__ void load_x16(const float* p, float2 (&xr)[16]) {
-  const float4* p4 = reinterpret_cast<const float4*>(p);
+// Staged x layout of one column: 8 planes of `plane` float4 each; float4 j of
+// block bi (floats 4j..4j+3 of the block's 32) sits at plane j, slot bi. Lanes
+// that read consecutive blocks therefore read consecutive 16-byte slots, which
+// keeps shared-memory accesses free of bank conflicts.
+__device__ __forceinline__ void load_x16(const float* col, int plane, int bi, float2 (&xr)[16]) {
+  const float4* p4 = reinterpret_cast<const float4*>(col) + bi;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float4 v = p4[i];
+    float4 v = p4[i * plane];
     xr[2 * i] = make_float2(v.x, v.y);
     xr[2 * i + 1] = make_float2(v.z, v.w);
   }
@@ -88,7 +92,8 @@ __device__ __forceinline__ void load_x16(const float* p, float2 (&xr)[16]) {
 // f32 in the consumption order of QT. One thread per 32-element block: its four
 // 16-byte loads are issued before any use, so a CTA pays about one global-load
 // latency per pass instead of one per element.
-__device__ __forceinline__ void stage_block(int qt, float* dst, const __half* src) {
+__device__ __forceinline__ void stage_block(int qt, float* col, int plane, int bi,
+                                            const __half* src) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
   const uint4 v0 = s4[0], v1 = s4[1], v2 = s4[2], v3 = s4[3];
   __align__(16) __half h[32];
@@ -101,18 +106,20 @@ __device__ __forceinline__ void stage_block(int qt, float* dst, const __half* sr
   for (int s = 0; s < 32; ++s)
     o[s] = qt == T_Q4_0 ? __half2float(h[q4_xorder_elem(s)]) * q4_xorder_scale(s)
                         : __half2float(h[s]);
-  float4* d4 = reinterpret_cast<float4*>(dst);
+  float4* d4 = reinterpret_cast<float4*>(col) + bi;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) d4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  for (int i = 0; i < 8; ++i) d4[i * plane] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
 }
 
+// Column c occupies xs[c * xstride ...] (xstride = 32 * plane floats).
 template <int QT, int NC>
 __device__ __forceinline__ void stage_x(float* xs, int xstride, const __half* x, int k,
                                         const int (&cols)[NC], int kb0, int kb1) {
   const int nbk = kb1 - kb0;
+  const int plane = xstride / QK;
   for (int it = threadIdx.x; it < NC * nbk; it += blockDim.x) {
     const int c = it / nbk, b = it % nbk;
-    stage_block(QT, xs + c * xstride + b * QK, x + (size_t)cols[c] * k + (size_t)(kb0 + b) * QK);
+    stage_block(QT, xs + c * xstride, plane, b, x + (size_t)cols[c] * k + (size_t)(kb0 + b) * QK);
   }
 }
 
@@ -125,8 +132,8 @@ __device__ __forceinline__ void cc_rowdot_1col(const uint8_t* __restrict__ qa,
                                                const uint8_t* __restrict__ qb,
                                                const uint16_t* __restrict__ sb,
                                                size_t rowbytes, int nb, const int (&rowidx)[RW],
-                                               const float* xs, int kb0, int kb1, int lane,
-                                               float (&ta)[RW], float (&tb)[RW]) {
+                                               const float* xs, int plane, int kb0, int kb1,
+                                               int lane, float (&ta)[RW], float (&tb)[RW]) {
   constexpr int QB = QTraits<QT>::QB;
   for (int b = kb0 + lane; b < kb1; b += 32) {
     Blk<QT> bqa[RW], bqb[RW];
@@ -141,7 +148,7 @@ __device__ __forceinline__ void cc_rowdot_1col(const uint8_t* __restrict__ qa,
       }
     }
     float2 xr[16];
-    load_x16(xs + (b - kb0) * QK, xr);
+    load_x16(xs, plane, b - kb0, xr);
 #pragma unroll
     for (int r = 0; r < RW; ++r) {
       ta[r] = fmaf(h2f(bsa[r]), blk_dot(bqa[r], xr), ta[r]);

@@ -110,7 +110,7 @@ __device__ __forceinline__ void stage_x_rt(int qt, float* xs, int xstride, const
   for (int it = threadIdx.x; it < ncols * nbk; it += blockDim.x) {
     const int c = it / nbk, b = it % nbk;
     if (!((cmask >> c) & 1u)) continue;
-    stage_block(qt, xs + c * xstride + b * QK, x + (size_t)c * colstride + (size_t)b * QK);
+    stage_block(qt, xs + c * xstride, xstride / QK, b, x + (size_t)c * colstride + (size_t)b * QK);
   }
 }
 
@@ -182,8 +182,8 @@ __global__ void __launch_bounds__(MOE_THREADS) moe_gate_up_kernel(const MoeDev p
       float ta[MOE_RW], tb[MOE_RW];
 #pragma unroll
       for (int r = 0; r < MOE_RW; ++r) { ta[r] = 0.f; tb[r] = 0.f; }
-      cc_rowdot_1col<QT, MOE_RW, true>(qa, sa, qb, sb, rowbytes, nb, rowidx, xs + c * k, 0, nb,
-                                       lane, ta, tb);
+      cc_rowdot_1col<QT, MOE_RW, true>(qa, sa, qb, sb, rowbytes, nb, rowidx, xs + c * k, nb, 0,
+                                       nb, lane, ta, tb);
       int idx, idx2;
       const float g = warp_transpose_reduce<MOE_RW>(ta, lane, idx);
       const float uu = warp_transpose_reduce<MOE_RW>(tb, lane, idx2);
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(MOE_THREADS) moe_down_kernel(const MoeDev p) {
 #pragma unroll
       for (int r = 0; r < MOE_RW; ++r) { ta[r] = 0.f; tb[r] = 0.f; }
       cc_rowdot_1col<QT, MOE_RW, false>(qa, sa, nullptr, nullptr, rowbytes, nb, rowidx,
-                                        xs + c * k, 0, nb, lane, ta, tb);
+                                        xs + c * k, nb, 0, nb, lane, ta, tb);
       int idx;
       const float v = warp_transpose_reduce<MOE_RW>(ta, lane, idx);
       if ((lane & (32 / MOE_RW - 1)) == 0) {
