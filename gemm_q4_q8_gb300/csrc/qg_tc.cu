@@ -39,7 +39,9 @@ namespace qg {
 constexpr int TC_BM = 64;                 // rows per CTA
 constexpr int TC_KT = 256;                // weights per stage (one K unit)
 constexpr int TC_CONSUMERS = 8;           // 4 m-tiles x 2 k-groups
-constexpr int TC_THREADS = (TC_CONSUMERS + 1) * 32;
+constexpr int TC_WARP_TMA = TC_CONSUMERS;     // issues the TMA copies
+constexpr int TC_WARP_XP = TC_CONSUMERS + 1;  // permutes x into B-fragment order
+constexpr int TC_THREADS = (TC_CONSUMERS + 2) * 32;
 constexpr int TC_SMEM_BUDGET = 112 * 1024;  // two CTAs per SM
 constexpr long long TC_WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before giving up
 
@@ -174,7 +176,6 @@ struct TcParams {
   int units;   // K / TC_KT
   int ksplit;  // CTAs per cluster along K
   int ns;      // pipeline stages
-  int nu_max;  // K units of the largest split
   const __half* x;
   const float* y0;
   float* y;
@@ -187,9 +188,11 @@ struct TcShape {
   static constexpr int QROW = QT == T_Q4_0 ? 128 : 256;  // quant bytes per row per unit
   static constexpr int A_BYTES = TC_BM * QROW;
   static constexpr int S_BYTES = TC_BM * 16;             // 8 f16 scales per row per unit
-  static constexpr int STAGE = NMAT * (A_BYTES + S_BYTES);
+  static constexpr int AS_BYTES = NMAT * (A_BYTES + S_BYTES);  // weights of one unit (TMA)
   static constexpr int CPAD = 8 * NT;
-  static constexpr int XP_UNIT = 8 * CPAD * 64;          // permuted x bytes per unit
+  static constexpr int X_BYTES = CPAD * TC_KT * 2;       // raw x of one unit (TMA), [CPAD][256] f16
+  static constexpr int B_BYTES = 8 * CPAD * 64;          // x of one unit in B-fragment order
+  static constexpr int STAGE = AS_BYTES + X_BYTES + B_BYTES;
   static constexpr int NF = 4 * NT * NMAT;               // accumulator floats per lane
   static constexpr int SLOT = 4 * 32 * NF * 4;           // one CTA's partial tile
 };
@@ -198,16 +201,16 @@ template <int QT, int NT, bool DUAL>
 __global__ void __launch_bounds__(TC_THREADS, 2)
 tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mS0,
           const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mS1,
-          const TcParams p) {
+          const __grid_constant__ CUtensorMap mX, const TcParams p) {
   using S = TcShape<QT, NT, DUAL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   const int ns = p.ns;
   uint8_t* stages = smem;
-  uint8_t* xperm = smem + (size_t)ns * S::STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(xperm + (size_t)p.nu_max * S::XP_UNIT);
-  uint64_t* empty = full + ns;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ns * S::STAGE);  // A, S, B ready
+  uint64_t* xfull = full + ns;                                                 // raw x landed
+  uint64_t* empty = xfull + ns;                                                // stage free
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = blockIdx.x % p.ksplit;
@@ -217,69 +220,67 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   const int u1 = (int)((long)(rank + 1) * p.units / p.ksplit);
   const int nu = u1 - u0;
 
+  // Stage layout: [A, S (weights, TMA)] [raw x (TMA)] [x in B-fragment order].
+  // full[s]: TMA bytes of A and S plus one arrival of the x-permuting warp;
+  // xfull[s]: TMA bytes of raw x; empty[s]: the 8 consumers and the x warp.
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], TC_CONSUMERS);
+      mbar_init(&full[s], 2);
+      mbar_init(&xfull[s], 1);
+      mbar_init(&empty[s], TC_CONSUMERS + 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  const bool producer = warp == TC_CONSUMERS;
-  uint64_t policy = 0;
-  auto issue = [&](int i) {  // stage i of this CTA's K range
-    const int s = i % ns;
-    uint8_t* st = stages + (size_t)s * S::STAGE;
-    mbar_expect_tx(&full[s], (uint32_t)S::STAGE);
-    const int u = u0 + i;
+  const bool producer = warp == TC_WARP_TMA;
+  const bool xwarp = warp == TC_WARP_XP;
+  if (producer) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      for (int i = 0; i < nu; ++i) {
+        const int s = i % ns;
+        if (i >= ns && !mbar_wait(&empty[s], (uint32_t)(((i / ns) - 1) & 1))) break;
+        uint8_t* st = stages + (size_t)s * S::STAGE;
+        const int u = u0 + i;
+        mbar_expect_tx(&xfull[s], (uint32_t)S::X_BYTES);
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(st + S::AS_BYTES)),
+            "l"(&mX), "r"(u * TC_KT), "r"(0), "r"(smem_u32(&xfull[s]))
+            : "memory");
+        mbar_expect_tx(&full[s], (uint32_t)S::AS_BYTES);
 #pragma unroll
-    for (int m = 0; m < S::NMAT; ++m) {
-      const CUtensorMap* mA = m == 0 ? &mA0 : &mA1;
-      const CUtensorMap* mS = m == 0 ? &mS0 : &mS1;
-      uint8_t* a = st + m * S::A_BYTES;
+        for (int m = 0; m < S::NMAT; ++m) {
+          const CUtensorMap* mA = m == 0 ? &mA0 : &mA1;
+          const CUtensorMap* mS = m == 0 ? &mS0 : &mS1;
+          uint8_t* a = st + m * S::A_BYTES;
 #pragma unroll
-      for (int bx = 0; bx < S::QROW / 128; ++bx)
-        tma_load_2d(a + bx * TC_BM * 128, mA, u * S::QROW + bx * 128, m0, &full[s], policy);
-      tma_load_2d(st + S::NMAT * S::A_BYTES + m * S::S_BYTES, mS, u * 8, m0, &full[s], policy);
-    }
-  };
-  if (producer && lane == 0) {
-    policy = policy_evict_first();
-    for (int i = 0; i < nu && i < ns; ++i) issue(i);
-  }
-
-  // Permute x for this CTA's K range: for block b, column c, lane slot t, the
-  // 16 bytes [x4t, x4t+2, x4t+1, x4t+3, x4t+16, x4t+18, x4t+17, x4t+19].
-  // Four items per thread per pass, all sixteen 16-byte loads issued first.
-  {
-    const int items = nu * 8 * S::CPAD;
-    for (int base = tid; base < items; base += 4 * TC_THREADS) {
-      uint4 q[4][4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int it = base + u * TC_THREADS;
-        const int b = it / S::CPAD, c = it % S::CPAD;
-        if (it < items && c < p.ncols) {
-          const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)c * p.k +
-                                                            (size_t)(u0 * 8 + b) * QK);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) q[u][v] = src[v];
-        } else {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) q[u][v] = make_uint4(0, 0, 0, 0);
+          for (int bx = 0; bx < S::QROW / 128; ++bx)
+            tma_load_2d(a + bx * TC_BM * 128, mA, u * S::QROW + bx * 128, m0, &full[s], pol_w);
+          tma_load_2d(st + S::NMAT * S::A_BYTES + m * S::S_BYTES, mS, u * 8, m0, &full[s], pol_w);
         }
       }
+    }
+    __syncwarp();
+  } else if (xwarp) {
+    // Permute each unit's raw x [CPAD][256] into B-fragment order: for block b,
+    // column c, lane slot t, the 16 bytes [x4t, x4t+2, x4t+1, x4t+3, x4t+16,
+    // x4t+18, x4t+17, x4t+19] of that block (columns >= ncols arrive as zeros).
+    for (int i = 0; i < nu; ++i) {
+      const int s = i % ns;
+      if (!mbar_wait(&xfull[s], (uint32_t)((i / ns) & 1))) break;
+      const uint8_t* xr = stages + (size_t)s * S::STAGE + S::AS_BYTES;
+      uint8_t* xb = stages + (size_t)s * S::STAGE + S::AS_BYTES + S::X_BYTES;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int it = base + u * TC_THREADS;
-        if (it >= items) continue;
-        const int b = it / S::CPAD, c = it % S::CPAD;
-        const uint32_t lo[8] = {q[u][0].x, q[u][0].y, q[u][0].z, q[u][0].w,
-                                q[u][1].x, q[u][1].y, q[u][1].z, q[u][1].w};
-        const uint32_t hi[8] = {q[u][2].x, q[u][2].y, q[u][2].z, q[u][2].w,
-                                q[u][3].x, q[u][3].y, q[u][3].z, q[u][3].w};
-        uint4* dst = reinterpret_cast<uint4*>(xperm + ((size_t)(b * S::CPAD + c) * 4) * 16);
+      for (int r = 0; r < (8 * S::CPAD) / 32; ++r) {
+        const int it = lane + 32 * r;
+        const int b = it & 7, c = it >> 3;
+        const uint4* src = reinterpret_cast<const uint4*>(xr + c * (TC_KT * 2) + b * 64);
+        const uint4 q0 = src[0], q1 = src[1], q2 = src[2], q3 = src[3];
+        const uint32_t lo[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const uint32_t hi[8] = {q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+        uint4* dst = reinterpret_cast<uint4*>(xb + ((b * S::CPAD + c) * 4) * 16);
 #pragma unroll
         for (int t = 0; t < 4; ++t)
           dst[t] = make_uint4(__byte_perm(lo[2 * t], lo[2 * t + 1], 0x5410),
@@ -287,9 +288,16 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
                               __byte_perm(hi[2 * t], hi[2 * t + 1], 0x5410),
                               __byte_perm(hi[2 * t], hi[2 * t + 1], 0x7632));
       }
+      // raw x was read through the generic proxy and is refilled by TMA
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&full[s]);
+        mbar_arrive(&empty[s]);
+      }
     }
+    __syncwarp();
   }
-  __syncthreads();
 
   const int mi = warp & 3, kj = (warp >> 2) & 1;
   const int g = lane >> 2, t = lane & 3;
@@ -301,114 +309,92 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[m][n][e] = 0.f;
 
-  if (producer) {
-    if (lane == 0) {
-      for (int i = ns; i < nu; ++i) {
-        const int s = i % ns;
-        if (!mbar_wait(&empty[s], (uint32_t)(((i / ns) - 1) & 1))) break;
-        issue(i);
-      }
-    }
-    __syncwarp();
-  } else {
-    const uint32_t xp_base = smem_u32(xperm);
-    // ldmatrix source row/chunk of this lane: lanes 0-7 rows 0-7 and lanes 8-15
-    // rows 8-15 of the m-tile at chunk c; lanes 16-31 the same rows at chunk c+1.
+  if (!producer && !xwarp) {
+    // k-group kj owns the four contiguous blocks 4kj..4kj+3 of every unit.
+    // ldmatrix source of this lane: lanes 0-7 rows 0-7 and lanes 8-15 rows 8-15
+    // of the m-tile at chunk c; lanes 16-31 the same rows at chunk c+1. The
+    // swizzled byte offsets depend only on the lane and k-group: computed once.
     const int lrow = mi * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
     const int lchunk = lane >> 4;
-    const uint32_t srow_g = (uint32_t)((mi * 16 + g) * 16);
-    const uint32_t srow_g8 = (uint32_t)((mi * 16 + g + 8) * 16);
+    uint32_t aoff[4];  // per block j of the k-group (Q4_0 uses j = 0 and 2)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int chunk, box;
+      if (QT == T_Q4_0) { chunk = 4 * kj + j + lchunk; box = 0; }   // pair (j, j+1) for j even
+      else { chunk = 2 * j + lchunk; box = kj; }                     // block 4kj + j in box kj
+      aoff[j] = (uint32_t)(box * TC_BM * 128 + lrow * 128 + ((chunk ^ (lrow & 7)) << 4));
+    }
+    const uint32_t soff_g = (uint32_t)((mi * 16 + g) * 16 + 8 * kj);
+    const uint32_t soff_g8 = (uint32_t)((mi * 16 + g + 8) * 16 + 8 * kj);
+    const uint32_t boff = (uint32_t)(S::AS_BYTES + S::X_BYTES + ((4 * kj * S::CPAD + g) * 4 + t) * 16);
     for (int i = 0; i < nu; ++i) {
       const int s = i % ns;
       if (!mbar_wait(&full[s], (uint32_t)((i / ns) & 1))) break;
       const uint32_t st = smem_u32(stages + (size_t)s * S::STAGE);
       const uint32_t sbase = st + S::NMAT * S::A_BYTES;
-      // the 8 f16 scales of rows g and g+8 for this unit, per matrix
-      uint4 sg4[S::NMAT], sg84[S::NMAT];
+      const uint32_t bbase = st + boff;
+      // the 4 f16 scales of rows g and g+8 for this k-group's blocks, per matrix
+      float dg[S::NMAT][4], dg8[S::NMAT][4];
 #pragma unroll
       for (int m = 0; m < S::NMAT; ++m) {
-        sg4[m] = lds128(sbase + m * S::S_BYTES + srow_g);
-        sg84[m] = lds128(sbase + m * S::S_BYTES + srow_g8);
+        uint32_t a0, a1, b0, b1;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a0), "=r"(a1) : "r"(sbase + m * S::S_BYTES + soff_g));
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(b0), "=r"(b1) : "r"(sbase + m * S::S_BYTES + soff_g8));
+        dg[m][0] = h2f((uint16_t)(a0 & 0xffffu)); dg[m][1] = h2f((uint16_t)(a0 >> 16));
+        dg[m][2] = h2f((uint16_t)(a1 & 0xffffu)); dg[m][3] = h2f((uint16_t)(a1 >> 16));
+        dg8[m][0] = h2f((uint16_t)(b0 & 0xffffu)); dg8[m][1] = h2f((uint16_t)(b0 >> 16));
+        dg8[m][2] = h2f((uint16_t)(b1 & 0xffffu)); dg8[m][3] = h2f((uint16_t)(b1 >> 16));
       }
+      // raw quant words of rows g and g+8 (Q4_0: blocks j, j+1 from one
+      // ldmatrix at even j; Q8_0: both 16-element halves of block j)
+      uint32_t W[S::NMAT][4];
 #pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
-        // Q4_0: blocks (c0, c0+1), c0 = 2kj + 4pr, from one ldmatrix.x4 per matrix.
-        // Q8_0: blocks kj + 4pr and kj + 4pr + 2, one ldmatrix.x4 each.
-        uint32_t W[S::NMAT][2][4];  // [matrix][block of the pair][r0..r3]
+      for (int j = 0; j < 4; ++j) {
 #pragma unroll
         for (int m = 0; m < S::NMAT; ++m) {
           const uint32_t abase = st + m * S::A_BYTES;
           if (QT == T_Q4_0) {
-            const int chunk = 2 * kj + 4 * pr + lchunk;
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(abase + (uint32_t)(lrow * 128 + ((chunk ^ (lrow & 7)) << 4)), r0, r1, r2, r3);
-            W[m][0][0] = r0; W[m][0][1] = r1; W[m][1][0] = r2; W[m][1][1] = r3;
-            W[m][0][2] = W[m][0][3] = W[m][1][2] = W[m][1][3] = 0;
-          } else {
-#pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-              const int blk = kj + 4 * pr + 2 * sub;
-              const int bx = blk >> 2, chunk = 2 * (blk & 3) + lchunk;
-              ldsm_x4(abase + (uint32_t)(bx * TC_BM * 128 + lrow * 128 + ((chunk ^ (lrow & 7)) << 4)),
-                      W[m][sub][0], W[m][sub][1], W[m][sub][2], W[m][sub][3]);
+            if ((j & 1) == 0) {
+              uint32_t r0, r1, r2, r3;
+              ldsm_x4(abase + aoff[j], r0, r1, r2, r3);
+              W[m][0] = r0; W[m][1] = r1; W[m][2] = r2; W[m][3] = r3;  // blocks j, j+1
             }
+          } else {
+            ldsm_x4(abase + aoff[j], W[m][0], W[m][1], W[m][2], W[m][3]);
           }
         }
+        uint4 bf[NT];
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-          const int blk = QT == T_Q4_0 ? (2 * kj + 4 * pr + sub) : (kj + 4 * pr + 2 * sub);
-          uint4 bf[NT];
+        for (int n = 0; n < NT; ++n) bf[n] = lds128(bbase + (uint32_t)((j * S::CPAD + n * 8) * 64));
 #pragma unroll
-          for (int n = 0; n < NT; ++n)
-            bf[n] = lds128(xp_base + (uint32_t)((((i * 8 + blk) * S::CPAD + n * 8 + g) * 4 + t) * 16));
+        for (int m = 0; m < S::NMAT; ++m) {
+          uint32_t A0[4], A1[4];
+          if (QT == T_Q4_0) {
+            const uint32_t wg = (j & 1) ? W[m][2] : W[m][0];
+            const uint32_t wg8 = (j & 1) ? W[m][3] : W[m][1];
+            uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
+            dq4_f16(wg, e0, e1, e2, e3);
+            dq4_f16(wg8, f0, f1, f2, f3);
+            A0[0] = e0; A0[1] = f0; A0[2] = e2; A0[3] = f2;
+            A1[0] = e1; A1[1] = f1; A1[2] = e3; A1[3] = f3;
+          } else {
+            uint32_t p0, p1, q0, q1;
+            dq8_f16(W[m][0], p0, p1);
+            dq8_f16(W[m][1], q0, q1);
+            A0[0] = p0; A0[1] = q0; A0[2] = p1; A0[3] = q1;
+            dq8_f16(W[m][2], p0, p1);
+            dq8_f16(W[m][3], q0, q1);
+            A1[0] = p0; A1[1] = q0; A1[2] = p1; A1[3] = q1;
+          }
 #pragma unroll
-          for (int m = 0; m < S::NMAT; ++m) {
-            uint32_t A0[4], A1[4];
-            if (QT == T_Q4_0) {
-              uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
-              dq4_f16(W[m][sub][0], e0, e1, e2, e3);
-              dq4_f16(W[m][sub][1], f0, f1, f2, f3);
-              A0[0] = e0; A0[1] = f0; A0[2] = e2; A0[3] = f2;
-              A1[0] = e1; A1[1] = f1; A1[2] = e3; A1[3] = f3;
-            } else {
-              uint32_t p0, p1, q0, q1;
-              dq8_f16(W[m][sub][0], p0, p1);
-              dq8_f16(W[m][sub][1], q0, q1);
-              A0[0] = p0; A0[1] = q0; A0[2] = p1; A0[3] = q1;
-              dq8_f16(W[m][sub][2], p0, p1);
-              dq8_f16(W[m][sub][3], q0, q1);
-              A1[0] = p0; A1[1] = q0; A1[2] = p1; A1[3] = q1;
-            }
-            // scale of block blk (word blk/2, half blk%2) without indexed registers:
-            // Q4_0: word kj + 2pr, half sub; Q8_0: word 2pr + sub, half kj.
-            uint32_t sw, sw8;
-            bool hi_half;
-            if (QT == T_Q4_0) {
-              const uint32_t a0 = pr ? sg4[m].z : sg4[m].x, a1 = pr ? sg4[m].w : sg4[m].y;
-              const uint32_t b0 = pr ? sg84[m].z : sg84[m].x, b1 = pr ? sg84[m].w : sg84[m].y;
-              sw = kj ? a1 : a0;
-              sw8 = kj ? b1 : b0;
-              hi_half = sub != 0;
-            } else {
-              const int wi = 2 * pr + sub;
-              sw = wi == 0 ? sg4[m].x : (wi == 1 ? sg4[m].y : (wi == 2 ? sg4[m].z : sg4[m].w));
-              sw8 = wi == 0 ? sg84[m].x : (wi == 1 ? sg84[m].y : (wi == 2 ? sg84[m].z : sg84[m].w));
-              hi_half = kj != 0;
-            }
-            const float dg = h2f((uint16_t)(hi_half ? (sw >> 16) : (sw & 0xffffu)));
-            const float dg8 = h2f((uint16_t)(hi_half ? (sw8 >> 16) : (sw8 & 0xffffu)));
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-              float fr[4];
-              mma16816(fr, A0, bf[n].x, bf[n].y);
-              mma16816_acc(fr, A1, bf[n].z, bf[n].w);
-              float2 lo = fma2(make_float2(dg, dg), make_float2(fr[0], fr[1]),
-                               make_float2(acc[m][n][0], acc[m][n][1]));
-              float2 hi = fma2(make_float2(dg8, dg8), make_float2(fr[2], fr[3]),
-                               make_float2(acc[m][n][2], acc[m][n][3]));
-              acc[m][n][0] = lo.x; acc[m][n][1] = lo.y;
-              acc[m][n][2] = hi.x; acc[m][n][3] = hi.y;
-            }
+          for (int n = 0; n < NT; ++n) {
+            float fr[4];
+            mma16816(fr, A0, bf[n].x, bf[n].y);
+            mma16816_acc(fr, A1, bf[n].z, bf[n].w);
+            acc[m][n][0] = fmaf(dg[m][j], fr[0], acc[m][n][0]);
+            acc[m][n][1] = fmaf(dg[m][j], fr[1], acc[m][n][1]);
+            acc[m][n][2] = fmaf(dg8[m][j], fr[2], acc[m][n][2]);
+            acc[m][n][3] = fmaf(dg8[m][j], fr[3], acc[m][n][3]);
           }
         }
       }
@@ -423,7 +409,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 
   // ---- reduce the two k-groups (fixed order: kj 0 + kj 1) in shared memory
   float* scratch = reinterpret_cast<float*>(stages);
-  if (!producer) {
+  if (!producer && !xwarp) {
     asm volatile("bar.sync 1, %0;" ::"n"(TC_CONSUMERS * 32) : "memory");
     if (kj == 1) {
       float* dst = scratch + (size_t)(mi * 32 + lane) * S::NF;
@@ -451,7 +437,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   // ---- reduce the cluster's K splits in rank order through distributed smem
   if (p.ksplit > 1) {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (!producer && kj == 0 && rank != 0) {
+    if (!producer && !xwarp && kj == 0 && rank != 0) {
       const uint32_t local = smem_u32(stages) +
                              (uint32_t)(((rank - 1) * 4 * 32 + mi * 32 + lane) * S::NF * 4);
       uint32_t remote;
@@ -469,7 +455,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
           }
     }
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (!producer && kj == 0 && rank == 0) {
+    if (!producer && !xwarp && kj == 0 && rank == 0) {
       for (int r = 1; r < p.ksplit; ++r) {
         const float* srcp = scratch + (size_t)(((r - 1) * 4 * 32) + mi * 32 + lane) * S::NF;
         int q = 0;
@@ -484,7 +470,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   }
 
   // ---- epilogue (rank 0, k-group 0)
-  if (producer || kj != 0 || rank != 0) return;
+  if (producer || xwarp || kj != 0 || rank != 0) return;
 #pragma unroll
   for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -536,32 +522,38 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
 }
 
 struct TcConfig {
-  int ksplit, ns, nu_max;
+  int ksplit, ns;
   size_t smem;
 };
 
 // Pinned per shape: depends only on (type, columns, dual, rows, k), never on
-// the device, so the reduction order is the same on every GPU.
+// the device, so the reduction order is the same on every GPU. The K split is
+// the largest that keeps every CTA in one wave of a fixed 304-CTA capacity
+// (two per SM on a 152-SM part): each CTA then streams as much K as possible,
+// which amortises its start-up and reduction. Stages: as many as fit, up to
+// the CTA's whole K range.
 template <int QT, int NT, bool DUAL>
 TcConfig pick_config_budget(int rows, int k, size_t budget) {
   using S = TcShape<QT, NT, DUAL>;
   const int units = k / TC_KT;
   const int ntile = (rows + TC_BM - 1) / TC_BM;
-  const int target = 304;  // CTAs that fill two per SM on a 152-SM part
-  TcConfig best{0, 0, 0, 0};
-  for (int ks = 1; ks <= 8 && ks <= units; ++ks) {
+  const int capacity = 304;
+  int ks = capacity / ntile;
+  if (ks > 8) ks = 8;
+  if (ks > units) ks = units;
+  if (ks < 1) ks = 1;
+  for (; ks >= 1; --ks) {
     const int nu_max = (units + ks - 1) / ks;
-    for (int ns = 6; ns >= 3; --ns) {
-      const size_t reuse = (size_t)ns * S::STAGE + (size_t)nu_max * S::XP_UNIT;
-      const size_t smem = 1024 + reuse + 2 * ns * sizeof(uint64_t);
-      if (smem > budget) continue;
-      if ((size_t)S::SLOT > reuse || (size_t)(ks - 1) * S::SLOT > reuse) continue;
-      best = {ks, ns, nu_max, smem};
-      break;
-    }
-    if (best.ksplit == ks && (long)ntile * ks >= target) break;
+    int ns = (int)((budget - 1024) / (S::STAGE + 3 * sizeof(uint64_t)));
+    if (ns > 8) ns = 8;
+    if (ns > nu_max) ns = nu_max;
+    if (ns < 2 && nu_max >= 2) continue;
+    if (ns < 1) continue;
+    const size_t reuse = (size_t)ns * S::STAGE;
+    if ((size_t)S::SLOT > reuse || (size_t)(ks - 1) * S::SLOT > reuse) continue;
+    return TcConfig{ks, ns, 1024 + reuse + 3 * ns * sizeof(uint64_t)};
   }
-  return best;
+  return TcConfig{0, 0, 0};
 }
 
 // Two CTAs per SM when the shape allows it, else one.
@@ -599,6 +591,12 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
     mA1 = mA0;
     mS1 = mS0;
   }
+  // x as a [ncols][k] f16 tensor; boxes of [CPAD rows][256 columns], rows past
+  // ncols read as zero
+  CUtensorMap mX;
+  if (!make_map(&mX, x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)k, (uint64_t)ncols, TC_KT,
+                S::CPAD, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   TcParams p{};
   p.rows = rows;
   p.k = k;
@@ -606,7 +604,6 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
   p.units = k / TC_KT;
   p.ksplit = cfg.ksplit;
   p.ns = cfg.ns;
-  p.nu_max = cfg.nu_max;
   p.x = reinterpret_cast<const __half*>(x);
   p.y0 = y0;
   p.y = y;
@@ -627,7 +624,7 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
   at[0].val.clusterDim.z = 1;
   lc.attrs = at;
   lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, kern, mA0, mS0, mA1, mS1, p);
+  e = cudaLaunchKernelEx(&lc, kern, mA0, mS0, mA1, mS1, mX, p);
   note_launch();
   (void)S::NF;
   return e != cudaSuccess ? e : cudaGetLastError();
