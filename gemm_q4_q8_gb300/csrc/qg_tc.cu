@@ -190,7 +190,7 @@ struct TcShape {
   static constexpr int S_BYTES = TC_BM * 16;             // 8 f16 scales per row per unit
   static constexpr int AS_BYTES = NMAT * (A_BYTES + S_BYTES);  // weights of one unit (TMA)
   static constexpr int CPAD = 8 * NT;
-  static constexpr int X_BYTES = CPAD * TC_KT * 2;       // raw x of one unit (TMA), [CPAD][256] f16
+  static constexpr int X_BYTES = CPAD * TC_KT * 2;       // raw x of one unit (TMA), [4][CPAD][64] f16
   static constexpr int B_BYTES = 8 * CPAD * 64;          // x of one unit in B-fragment order
   static constexpr int STAGE = AS_BYTES + X_BYTES + B_BYTES;
   static constexpr int NF = 4 * NT * NMAT;               // accumulator floats per lane
@@ -238,17 +238,19 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   if (producer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
-      for (int i = 0; i < nu; ++i) {
-        const int s = i % ns;
-        if (i >= ns && !mbar_wait(&empty[s], (uint32_t)(((i / ns) - 1) & 1))) break;
+      // stage s and phase bit ph advance incrementally (no division in the loop)
+      for (int i = 0, s = 0, ph = 0; i < nu; ++i, s = s + 1 == ns ? 0 : s + 1, ph ^= s == 0) {
+        if (i >= ns && !mbar_wait(&empty[s], (uint32_t)(ph ^ 1))) break;
         uint8_t* st = stages + (size_t)s * S::STAGE;
         const int u = u0 + i;
         mbar_expect_tx(&xfull[s], (uint32_t)S::X_BYTES);
-        asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(st + S::AS_BYTES)),
-            "l"(&mX), "r"(u * TC_KT), "r"(0), "r"(smem_u32(&xfull[s]))
-            : "memory");
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          asm volatile(
+              "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+              " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(st + S::AS_BYTES + q * S::CPAD * 128)),
+              "l"(&mX), "r"(u * TC_KT + q * 64), "r"(0), "r"(smem_u32(&xfull[s]))
+              : "memory");
         mbar_expect_tx(&full[s], (uint32_t)S::AS_BYTES);
 #pragma unroll
         for (int m = 0; m < S::NMAT; ++m) {
@@ -264,29 +266,37 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     }
     __syncwarp();
   } else if (xwarp) {
-    // Permute each unit's raw x [CPAD][256] into B-fragment order: for block b,
-    // column c, lane slot t, the 16 bytes [x4t, x4t+2, x4t+1, x4t+3, x4t+16,
-    // x4t+18, x4t+17, x4t+19] of that block (columns >= ncols arrive as zeros).
-    for (int i = 0; i < nu; ++i) {
-      const int s = i % ns;
-      if (!mbar_wait(&xfull[s], (uint32_t)((i / ns) & 1))) break;
+    // Permute each unit's raw x into B-fragment order: for block b, column c,
+    // lane slot t, the 16 bytes [x4t, x4t+2, x4t+1, x4t+3, x4t+16, x4t+18,
+    // x4t+17, x4t+19] of that block (columns >= ncols arrive as zeros). Raw x
+    // lands as four [CPAD][64] boxes with the 128-byte swizzle (16-byte chunk q
+    // of row c at chunk q ^ (c & 7)), and slot t of (b, c) is stored at
+    // position (t + (c >> 1)) & 3: both make this warp's loads and stores, and
+    // the consumers' fragment loads, free of bank conflicts.
+    for (int i = 0, s = 0, ph = 0; i < nu; ++i, s = s + 1 == ns ? 0 : s + 1, ph ^= s == 0) {
+      if (!mbar_wait(&xfull[s], (uint32_t)ph)) break;
       const uint8_t* xr = stages + (size_t)s * S::STAGE + S::AS_BYTES;
       uint8_t* xb = stages + (size_t)s * S::STAGE + S::AS_BYTES + S::X_BYTES;
 #pragma unroll
       for (int r = 0; r < (8 * S::CPAD) / 32; ++r) {
         const int it = lane + 32 * r;
-        const int b = it & 7, c = it >> 3;
-        const uint4* src = reinterpret_cast<const uint4*>(xr + c * (TC_KT * 2) + b * 64);
-        const uint4 q0 = src[0], q1 = src[1], q2 = src[2], q3 = src[3];
+        const int c = it & (S::CPAD - 1), b = it / S::CPAD;
+        const uint8_t* row = xr + (b >> 1) * (S::CPAD * 128) + c * 128;
+        const int q0i = (b & 1) * 4;
+        const uint4 q0 = *reinterpret_cast<const uint4*>(row + (((q0i + 0) ^ (c & 7)) << 4));
+        const uint4 q1 = *reinterpret_cast<const uint4*>(row + (((q0i + 1) ^ (c & 7)) << 4));
+        const uint4 q2 = *reinterpret_cast<const uint4*>(row + (((q0i + 2) ^ (c & 7)) << 4));
+        const uint4 q3 = *reinterpret_cast<const uint4*>(row + (((q0i + 3) ^ (c & 7)) << 4));
         const uint32_t lo[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         const uint32_t hi[8] = {q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
-        uint4* dst = reinterpret_cast<uint4*>(xb + ((b * S::CPAD + c) * 4) * 16);
+        uint8_t* dst = xb + (b * S::CPAD + c) * 64;
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-          dst[t] = make_uint4(__byte_perm(lo[2 * t], lo[2 * t + 1], 0x5410),
-                              __byte_perm(lo[2 * t], lo[2 * t + 1], 0x7632),
-                              __byte_perm(hi[2 * t], hi[2 * t + 1], 0x5410),
-                              __byte_perm(hi[2 * t], hi[2 * t + 1], 0x7632));
+          *reinterpret_cast<uint4*>(dst + (((t + (c >> 1)) & 3) << 4)) =
+              make_uint4(__byte_perm(lo[2 * t], lo[2 * t + 1], 0x5410),
+                         __byte_perm(lo[2 * t], lo[2 * t + 1], 0x7632),
+                         __byte_perm(hi[2 * t], hi[2 * t + 1], 0x5410),
+                         __byte_perm(hi[2 * t], hi[2 * t + 1], 0x7632));
       }
       // raw x was read through the generic proxy and is refilled by TMA
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -326,10 +336,10 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     }
     const uint32_t soff_g = (uint32_t)((mi * 16 + g) * 16 + 8 * kj);
     const uint32_t soff_g8 = (uint32_t)((mi * 16 + g + 8) * 16 + 8 * kj);
-    const uint32_t boff = (uint32_t)(S::AS_BYTES + S::X_BYTES + ((4 * kj * S::CPAD + g) * 4 + t) * 16);
-    for (int i = 0; i < nu; ++i) {
-      const int s = i % ns;
-      if (!mbar_wait(&full[s], (uint32_t)((i / ns) & 1))) break;
+    const uint32_t boff =
+        (uint32_t)(S::AS_BYTES + S::X_BYTES + ((4 * kj * S::CPAD + g) * 4 + ((t + (g >> 1)) & 3)) * 16);
+    for (int i = 0, s = 0, ph = 0; i < nu; ++i, s = s + 1 == ns ? 0 : s + 1, ph ^= s == 0) {
+      if (!mbar_wait(&full[s], (uint32_t)ph)) break;
       const uint32_t st = smem_u32(stages + (size_t)s * S::STAGE);
       const uint32_t sbase = st + S::NMAT * S::A_BYTES;
       const uint32_t bbase = st + boff;
@@ -345,58 +355,79 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         dg8[m][0] = h2f((uint16_t)(b0 & 0xffffu)); dg8[m][1] = h2f((uint16_t)(b0 >> 16));
         dg8[m][2] = h2f((uint16_t)(b1 & 0xffffu)); dg8[m][3] = h2f((uint16_t)(b1 >> 16));
       }
-      // raw quant words of rows g and g+8 (Q4_0: blocks j, j+1 from one
-      // ldmatrix at even j; Q8_0: both 16-element halves of block j)
-      uint32_t W[S::NMAT][4];
+      // All shared-memory reads of the stage are issued first: the raw quant
+      // words of rows g and g+8 (Q4_0: one ldmatrix covers blocks j, j+1;
+      // Q8_0: one covers both 16-element halves of block j) and the B
+      // fragments of the four blocks.
+      constexpr int NL = QT == T_Q4_0 ? 2 : 4;
+      uint32_t W[S::NMAT][NL][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int m = 0; m < S::NMAT; ++m)
 #pragma unroll
-        for (int m = 0; m < S::NMAT; ++m) {
-          const uint32_t abase = st + m * S::A_BYTES;
-          if (QT == T_Q4_0) {
-            if ((j & 1) == 0) {
-              uint32_t r0, r1, r2, r3;
-              ldsm_x4(abase + aoff[j], r0, r1, r2, r3);
-              W[m][0] = r0; W[m][1] = r1; W[m][2] = r2; W[m][3] = r3;  // blocks j, j+1
+        for (int l = 0; l < NL; ++l)
+          ldsm_x4(st + m * S::A_BYTES + aoff[QT == T_Q4_0 ? 2 * l : l], W[m][l][0], W[m][l][1],
+                  W[m][l][2], W[m][l][3]);
+      uint4 bf[4][NT];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) bf[j][n] = lds128(bbase + (uint32_t)((j * S::CPAD + n * 8) * 64));
+      // Then the blocks in groups of JB, so that every group carries four
+      // independent mma chains whatever the tile shape.
+      constexpr int JB = 4 / (S::NMAT * NT) > 0 ? 4 / (S::NMAT * NT) : 1;
+#pragma unroll
+      for (int jb = 0; jb < 4; jb += JB) {
+        uint32_t A0[JB][S::NMAT][4], A1[JB][S::NMAT][4];
+#pragma unroll
+        for (int jj = 0; jj < JB; ++jj)
+#pragma unroll
+          for (int m = 0; m < S::NMAT; ++m) {
+            const int j = jb + jj;
+            if (QT == T_Q4_0) {
+              const uint32_t wg = W[m][j >> 1][(j & 1) ? 2 : 0];
+              const uint32_t wg8 = W[m][j >> 1][(j & 1) ? 3 : 1];
+              uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
+              dq4_f16(wg, e0, e1, e2, e3);
+              dq4_f16(wg8, f0, f1, f2, f3);
+              A0[jj][m][0] = e0; A0[jj][m][1] = f0; A0[jj][m][2] = e2; A0[jj][m][3] = f2;
+              A1[jj][m][0] = e1; A1[jj][m][1] = f1; A1[jj][m][2] = e3; A1[jj][m][3] = f3;
+            } else {
+              uint32_t p0, p1, q0, q1;
+              dq8_f16(W[m][j][0], p0, p1);
+              dq8_f16(W[m][j][1], q0, q1);
+              A0[jj][m][0] = p0; A0[jj][m][1] = q0; A0[jj][m][2] = p1; A0[jj][m][3] = q1;
+              dq8_f16(W[m][j][2], p0, p1);
+              dq8_f16(W[m][j][3], q0, q1);
+              A1[jj][m][0] = p0; A1[jj][m][1] = q0; A1[jj][m][2] = p1; A1[jj][m][3] = q1;
             }
-          } else {
-            ldsm_x4(abase + aoff[j], W[m][0], W[m][1], W[m][2], W[m][3]);
           }
-        }
-        uint4 bf[NT];
+        float fr[JB][S::NMAT][NT][4];
 #pragma unroll
-        for (int n = 0; n < NT; ++n) bf[n] = lds128(bbase + (uint32_t)((j * S::CPAD + n * 8) * 64));
+        for (int jj = 0; jj < JB; ++jj)
 #pragma unroll
-        for (int m = 0; m < S::NMAT; ++m) {
-          uint32_t A0[4], A1[4];
-          if (QT == T_Q4_0) {
-            const uint32_t wg = (j & 1) ? W[m][2] : W[m][0];
-            const uint32_t wg8 = (j & 1) ? W[m][3] : W[m][1];
-            uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
-            dq4_f16(wg, e0, e1, e2, e3);
-            dq4_f16(wg8, f0, f1, f2, f3);
-            A0[0] = e0; A0[1] = f0; A0[2] = e2; A0[3] = f2;
-            A1[0] = e1; A1[1] = f1; A1[2] = e3; A1[3] = f3;
-          } else {
-            uint32_t p0, p1, q0, q1;
-            dq8_f16(W[m][0], p0, p1);
-            dq8_f16(W[m][1], q0, q1);
-            A0[0] = p0; A0[1] = q0; A0[2] = p1; A0[3] = q1;
-            dq8_f16(W[m][2], p0, p1);
-            dq8_f16(W[m][3], q0, q1);
-            A1[0] = p0; A1[1] = q0; A1[2] = p1; A1[3] = q1;
-          }
+          for (int m = 0; m < S::NMAT; ++m)
 #pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            float fr[4];
-            mma16816(fr, A0, bf[n].x, bf[n].y);
-            mma16816_acc(fr, A1, bf[n].z, bf[n].w);
-            acc[m][n][0] = fmaf(dg[m][j], fr[0], acc[m][n][0]);
-            acc[m][n][1] = fmaf(dg[m][j], fr[1], acc[m][n][1]);
-            acc[m][n][2] = fmaf(dg8[m][j], fr[2], acc[m][n][2]);
-            acc[m][n][3] = fmaf(dg8[m][j], fr[3], acc[m][n][3]);
-          }
-        }
+            for (int n = 0; n < NT; ++n)
+              mma16816(fr[jj][m][n], A0[jj][m], bf[jb + jj][n].x, bf[jb + jj][n].y);
+#pragma unroll
+        for (int jj = 0; jj < JB; ++jj)
+#pragma unroll
+          for (int m = 0; m < S::NMAT; ++m)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+              mma16816_acc(fr[jj][m][n], A1[jj][m], bf[jb + jj][n].z, bf[jb + jj][n].w);
+#pragma unroll
+        for (int jj = 0; jj < JB; ++jj)
+#pragma unroll
+          for (int m = 0; m < S::NMAT; ++m)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              const int j = jb + jj;
+              acc[m][n][0] = fmaf(dg[m][j], fr[jj][m][n][0], acc[m][n][0]);
+              acc[m][n][1] = fmaf(dg[m][j], fr[jj][m][n][1], acc[m][n][1]);
+              acc[m][n][2] = fmaf(dg8[m][j], fr[jj][m][n][2], acc[m][n][2]);
+              acc[m][n][3] = fmaf(dg8[m][j], fr[jj][m][n][3], acc[m][n][3]);
+            }
       }
       // The stage was read through the generic proxy (ldmatrix / ld.shared) and
       // is refilled by TMA through the async proxy: order the reads before the
@@ -591,11 +622,11 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
     mA1 = mA0;
     mS1 = mS0;
   }
-  // x as a [ncols][k] f16 tensor; boxes of [CPAD rows][256 columns], rows past
-  // ncols read as zero
+  // x as a [ncols][k] f16 tensor; boxes of [CPAD rows][64 columns] with the
+  // 128-byte swizzle, rows past ncols read as zero
   CUtensorMap mX;
-  if (!make_map(&mX, x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)k, (uint64_t)ncols, TC_KT,
-                S::CPAD, CU_TENSOR_MAP_SWIZZLE_NONE))
+  if (!make_map(&mX, x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)k, (uint64_t)ncols, 64,
+                S::CPAD, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams p{};
   p.rows = rows;
