@@ -153,7 +153,7 @@ qg_status qmoe_experts(qg_type t, const void* qg, const uint16_t* sg, const void
                        int32_t* uniq_ids_out, cudaStream_t stream) {
   if (!valid_type((int)t)) return QG_ERR_TYPE;
   if (n_expert < 1 || ffn <= 0 || hidden <= 0 || (ffn % 32) || (hidden % 32) || ncols < 1 ||
-      ncols > 8 || topk < 1 || topk > 16 || !qg::moe_shape_supported(ffn, hidden, ncols))
+      ncols > 8 || topk < 1 || topk > 16 || !qg::moe_shape_supported(ffn, hidden, ncols, topk))
     return QG_ERR_SHAPE;
   if (!qg || !sg || !qu || !su || !qd || !sd || !ids || !rw || !x || !y) return QG_ERR_NULL;
   const void* p16[] = {qg, sg, qu, su, qd, sd, x};

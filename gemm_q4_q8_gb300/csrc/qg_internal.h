@@ -53,7 +53,7 @@ struct MoeArgs {
   int32_t* uniq_out;
 };
 size_t moe_ws_bytes(int n_expert, int ffn, int hidden, int ncols, int topk);
-bool moe_shape_supported(int ffn, int hidden, int ncols);
+bool moe_shape_supported(int ffn, int hidden, int ncols, int topk);
 cudaError_t moe_forward(const MoeArgs& a, cudaStream_t s);
 
 cudaError_t repack_launch(int qt, const void* gguf, int rows, int k, void* q_out,

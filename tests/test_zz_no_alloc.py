@@ -70,9 +70,10 @@ def test_noalloc_rejects_problems_beyond_its_workspace():
     from gemm_q4_q8_gb300 import build
     build.build()
     L = qg.load()
-    # 16 columns is out of range for any MoE call; a large layer exceeds 8 MiB
-    assert qg.qmoe_workspace_bytes(256, 4096, 8192, 8, 16) > qg.QG_MOE_NOALLOC_WS_BYTES
+    # the workspace holds h for every (column, k) slot: a very wide expert FFN
+    # at 8 columns and top-16 exceeds 8 MiB
+    assert qg.qmoe_workspace_bytes(256, 32768, 1024, 8, 16) > qg.QG_MOE_NOALLOC_WS_BYTES
     st = L.qmoe_experts_noalloc(8, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 256,
-                                4096, 8192, 0x10000, 0x10000, 16, None, 0x10000, 8, None,
+                                32768, 1024, 0x10000, 0x10000, 16, None, 0x10000, 8, None,
                                 0x10000, None, None, None)
     assert st == 5  # QG_ERR_WORKSPACE, nothing launched
