@@ -23,6 +23,21 @@ template <> struct QTraits<T_Q8_0> { static constexpr int QB = 32; };
 constexpr uint32_t MAGIC_2P23 = 0x4B000000u;
 constexpr float F_2P23 = 8388608.0f;
 
+// The same pattern (and 1024 twice as f16x2) in constant memory. Read from
+// there, the pattern reaches the dequantisers as a register that the compiler
+// cannot fold into an immediate, so each (w & mask) | pattern below stays one
+// three-input logic instruction (a logic op takes one immediate at most).
+static __constant__ uint32_t c_or_f32 = 0x4B000000u;
+static __constant__ uint32_t c_or_f16x2 = 0x64006400u;
+
+// (a & MASK) | orv as one lop3 (truth table 0xEA = (A & B) | C).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t orv) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(orv));
+  return d;
+}
+
 // ---------------------------------------------------------------- loads
 // Weights are read once per call: read-only path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
@@ -89,10 +104,11 @@ __device__ __forceinline__ Q4Word dequant_q4_word(uint32_t w) {
   const float2 off_lo = make_float2(F_2P23 + 8.f, F_2P23 + 128.f);
   const float2 off_hi = make_float2(F_2P23 + 2048.f, F_2P23 + 32768.f);
   Q4Word r;
-  r.p0 = sub2(make_float2(u2f((w & 0x000Fu) | MAGIC_2P23), u2f((w & 0x00F0u) | MAGIC_2P23)), off_lo);
-  r.p1 = sub2(make_float2(u2f((w & 0x0F00u) | MAGIC_2P23), u2f((w & 0xF000u) | MAGIC_2P23)), off_hi);
-  r.p2 = sub2(make_float2(u2f((w16 & 0x000Fu) | MAGIC_2P23), u2f((w16 & 0x00F0u) | MAGIC_2P23)), off_lo);
-  r.p3 = sub2(make_float2(u2f((w16 & 0x0F00u) | MAGIC_2P23), u2f((w16 & 0xF000u) | MAGIC_2P23)), off_hi);
+  const uint32_t m = c_or_f32;
+  r.p0 = sub2(make_float2(u2f(and_or<0x000Fu>(w, m)), u2f(and_or<0x00F0u>(w, m))), off_lo);
+  r.p1 = sub2(make_float2(u2f(and_or<0x0F00u>(w, m)), u2f(and_or<0xF000u>(w, m))), off_hi);
+  r.p2 = sub2(make_float2(u2f(and_or<0x000Fu>(w16, m)), u2f(and_or<0x00F0u>(w16, m))), off_lo);
+  r.p3 = sub2(make_float2(u2f(and_or<0x0F00u>(w16, m)), u2f(and_or<0xF000u>(w16, m))), off_hi);
   return r;
 }
 

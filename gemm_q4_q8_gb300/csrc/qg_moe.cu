@@ -186,16 +186,25 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_down_kernel(const MoeDev p
   const int nparts = gridDim.x / p.ncols;
   const int c = blockIdx.x % p.ncols, part = blockIdx.x / p.ncols;
   if (part >= nparts) return;  // uniform over the CTA
-  if (t == 0) {
-    int m = 0;
-    for (int j = 0; j < p.topk; ++j) {
-      const int id = p.ids[c * p.topk + j];
-      if (id >= 0 && id < p.n_expert) {
-        s_e[m] = id; s_j[m] = j; s_w[m] = p.rw[c * p.topk + j]; ++m;
-      }
+  if (warp == 0) {
+    // live entries of column c in k order (one load per lane, then a ballot)
+    int id = -1;
+    float w = 0.f;
+    if (lane < p.topk) {
+      id = p.ids[c * p.topk + lane];
+      w = p.rw[c * p.topk + lane];
     }
-    if (p.has_shared) { s_e[m] = p.n_expert; s_j[m] = p.topk; s_w[m] = 1.f; ++m; }
-    s_nj = m;
+    const bool live = lane < p.topk && id >= 0 && id < p.n_expert;
+    const unsigned m = __ballot_sync(0xffffffffu, live);
+    if (live) {
+      const int at = __popc(m & ((1u << lane) - 1u));
+      s_e[at] = id; s_j[at] = lane; s_w[at] = w;
+    }
+    const int nl = __popc(m);
+    if (lane == 0) {
+      if (p.has_shared) { s_e[nl] = p.n_expert; s_j[nl] = p.topk; s_w[nl] = 1.f; }
+      s_nj = nl + (p.has_shared ? 1 : 0);
+    }
   }
   __syncthreads();
   const int nj = s_nj;

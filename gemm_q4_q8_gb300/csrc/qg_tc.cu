@@ -152,14 +152,14 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) 
 __device__ __forceinline__ void dq4_f16(uint32_t w, uint32_t& e0, uint32_t& e1, uint32_t& e2,
                                         uint32_t& e3) {
   const uint32_t w8 = w >> 8;
-  const uint32_t M = 0x64006400u;
+  const uint32_t M = c_or_f16x2;
   const uint32_t k1032 = 0x64086408u;  // 1032 = 1024 + 8
   const uint32_t k16th = 0x2C002C00u;  // 1/16
   const uint32_t km72 = 0xD480D480u;   // -72
-  e0 = hsub2_u((w & 0x000F000Fu) | M, k1032);
-  e2 = hsub2_u((w8 & 0x000F000Fu) | M, k1032);
-  e1 = hfma2_u((w & 0x00F000F0u) | M, k16th, km72);   // (1024 + 16 q) / 16 - 72 = q - 8
-  e3 = hfma2_u((w8 & 0x00F000F0u) | M, k16th, km72);
+  e0 = hsub2_u(and_or<0x000F000Fu>(w, M), k1032);
+  e2 = hsub2_u(and_or<0x000F000Fu>(w8, M), k1032);
+  e1 = hfma2_u(and_or<0x00F000F0u>(w, M), k16th, km72);   // (1024 + 16 q) / 16 - 72 = q - 8
+  e3 = hfma2_u(and_or<0x00F000F0u>(w8, M), k16th, km72);
 }
 // Q8_0: word w = int8 elements 4t..4t+3 of a 16-element half block:
 //   p0 = (el 4t, 4t+2), p1 = (4t+1, 4t+3), exactly q.
