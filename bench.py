@@ -399,33 +399,65 @@ def main(argv=None):
         gs.step(stream)
     torch.cuda.synchronize()
 
-    # ---- device-resident timed region, per-kernel events on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
-          for _ in range(args.steps)]
+    # The step is captured once into a CUDA graph (the library's calls are
+    # capture-safe: no allocation, no synchronisation) and the timed region
+    # replays it, so no per-call host work sits between the kernels.
+    cap = torch.cuda.Stream()
+    step_graph = torch.cuda.CUDAGraph()
+    l_before = qg.qg_kernel_launches()
+    with torch.cuda.graph(step_graph, stream=cap):
+        gs.step(cap)
+    launches_per_step = qg.qg_kernel_launches() - l_before
+    # Each call also gets a graph of its own, for the per-kernel breakdown:
+    # replayed back to back with a CUDA event between consecutive graphs.
+    graphs = []
+    for name in KERNELS:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            gs.call(name, cap)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step_graph.replay()
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region: whole-step graph replays
     clk = ClockSampler(local)
     clk.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    l0 = qg.qg_kernel_launches()
     t_wall0 = time.time()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        gs.step(stream, ev[i])
+        step_graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
-    launches = qg.qg_kernel_launches() - l0
+    launches = launches_per_step * args.steps
     if world > 1:
         torch.distributed.barrier()
     clk.stop()
     region_ms = e0.elapsed_time(e1)
     region_ms = max_over_ranks(region_ms, world, torch, device)
     ms_per_step = region_ms / args.steps
+
+    # ---- per-kernel breakdown: per-call graphs with events between them
+    nb_steps = max(3, min(args.steps, 50))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
+          for _ in range(nb_steps)]
+    for i in range(nb_steps):
+        for j, g in enumerate(graphs):
+            ev[i][j].record(stream)
+            g.replay()
+        ev[i][len(KERNELS)].record(stream)
+    torch.cuda.synchronize()
     per_kernel_ms = {name: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1])
-                                          for i in range(args.steps)]))
+                                          for i in range(nb_steps)]))
                      for j, name in enumerate(KERNELS)}
 
     # ---- end to end through the public API from pinned host buffers
@@ -482,6 +514,9 @@ def main(argv=None):
                 "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": e2e_ms},
         "gpu_launches": int(launches),
+        "timing": "value: one CUDA graph per step (all calls), replayed back to back; "
+                  "breakdown: one graph per call, replayed back to back with a CUDA event "
+                  "between consecutive graphs (includes each graph's launch gap)",
         "clocks": clk.summary(t_wall0, t_wall1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
