@@ -96,22 +96,34 @@ class GpuStep:
         def d(a):
             return t.from_numpy(np.ascontiguousarray(a)).cuda()
 
-        def d16(a):  # uint16 bit patterns -> int16 storage
-            return t.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+        def dq(qtype, q, scl):
+            # load-time repack on the GPU: GGUF blocks -> the library's layout
+            rows, nb = scl.shape
+            blocks = d(synth.to_gguf_blocks(qtype, q, scl))
+            qd = t.empty(q.shape, dtype=t.uint8, device="cuda")
+            sd = t.empty(scl.shape, dtype=t.int16, device="cuda")
+            qg.qrepack(qtype, blocks, rows, nb * 32, qd, sd)
+            t.cuda.synchronize()
+            del blocks
+            return qd, sd
 
         g = w["gemv"]
-        self.g_q, self.g_s = d(g["q"]), d16(g["scl"])
+        self.g_q, self.g_s = dq(synth.Q4_0, g["q"], g["scl"])
         l = w["lmhead"]
-        self.l_q, self.l_s = d(l["q"]), d16(l["scl"])
+        self.l_q, self.l_s = dq(synth.Q8_0, l["q"], l["scl"])
         tw = w["twins"]
-        self.t_q, self.t_s = d(tw["q"]), d16(tw["scl"])
+        self.t_q, self.t_s = dq(synth.Q4_0, tw["q"], tw["scl"])
         f = w["ffn"]
-        self.f_qg, self.f_sg, self.f_qu, self.f_su = d(f["qg"]), d16(f["sg"]), d(f["qu"]), d16(f["su"])
-        self.f_qd, self.f_sd = d(f["qd"]), d16(f["sd"])
+        self.f_qg, self.f_sg = dq(f["qtype"], f["qg"], f["sg"])
+        self.f_qu, self.f_su = dq(f["qtype"], f["qu"], f["su"])
+        self.f_qd, self.f_sd = dq(f["qtype"], f["qd"], f["sd"])
         m = w["moe"]
-        self.m = {k: (d16(m[k]) if k in ("sg", "su", "sd") else d(m[k])) for k in
-                  ("qg", "sg", "qu", "su", "qd", "sd")}
-        self.m_sh = {k: (d16(v) if k.startswith("s") else d(v)) for k, v in m["shared"].items()}
+        self.m = {}
+        for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
+            self.m[a], self.m[b] = dq(m["qtype"], m[a], m[b])
+        self.m_sh = {}
+        for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
+            self.m_sh[a], self.m_sh[b] = dq(m["qtype"], m["shared"][a], m["shared"][b])
         ws = qg.qmoe_workspace_bytes(m["n_expert"], m["ffn"], m["hidden"], m["ncols"], m["topk"])
         self.m_ws = t.empty(ws, dtype=t.uint8, device="cuda")
         self.m_err = t.zeros(1, dtype=t.int32, device="cuda")

@@ -105,7 +105,7 @@ __device__ __forceinline__ void stage_block(int qt, float* col, int plane, int b
 #pragma unroll
   for (int s = 0; s < 32; ++s)
     o[s] = qt == T_Q4_0 ? __half2float(h[q4_xorder_elem(s)]) * q4_xorder_scale(s)
-                        : __half2float(h[s]);
+                        : __half2float(h[q8_xorder_elem(s)]);
   float4* d4 = reinterpret_cast<float4*>(col) + bi;
 #pragma unroll
   for (int i = 0; i < 8; ++i) d4[i * plane] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);

@@ -112,14 +112,23 @@ __device__ __forceinline__ Q4Word dequant_q4_word(uint32_t w) {
   return r;
 }
 
-// Pre-scaled x layout for one Q4_0 block (32 floats) in consumption order:
-// for word i (bytes 4i..4i+3), 8 floats:
-//   x[4i]*1, x[4i+16]/16, x[4i+1]/256, x[4i+17]/4096,
-//   x[4i+2]*1, x[4i+18]/16, x[4i+3]/256, x[4i+19]/4096
+// GGUF byte of a 16-byte group held by stored byte sb of that group: the two
+// 8-byte halves are interleaved, stored byte 2m + h = GGUF byte m + 8h.
+__host__ __device__ __forceinline__ int gguf_byte_of_stored(int sb) { return (sb >> 1) + 8 * (sb & 1); }
+
+// Pre-scaled x layout for one Q4_0 block (32 floats) in consumption order: for
+// word i (stored bytes 4i..4i+3, GGUF bytes g0..g3 = 2i, 2i+8, 2i+1, 2i+9), 8
+// floats: x[g0]*1, x[g0+16]/16, x[g1]/256, x[g1+16]/4096, x[g2]*1,
+// x[g2+16]/16, x[g3]/256, x[g3+16]/4096 (GGUF byte g holds elements g, g+16).
 __host__ __device__ __forceinline__ int q4_xorder_elem(int s) {
-  int i = s >> 3, j = s & 7;
-  int byte = 4 * i + (j >> 1);
+  const int i = s >> 3, j = s & 7;
+  const int byte = gguf_byte_of_stored(4 * i + (j >> 1));
   return (j & 1) ? byte + 16 : byte;
+}
+// Q8_0 x order: slot s takes the element of stored byte s (word s/4 gives the
+// float pairs (byte 0, byte 1) and (byte 2, byte 3)).
+__host__ __device__ __forceinline__ int q8_xorder_elem(int s) {
+  return (s & ~15) + gguf_byte_of_stored(s & 15);
 }
 __device__ __forceinline__ float q4_xorder_scale(int s) {
   // j = s & 7: 0 -> 1, 1 -> 1/16, 2 -> 1/256, 3 -> 1/4096, 4 -> 1, ...
@@ -128,7 +137,8 @@ __device__ __forceinline__ float q4_xorder_scale(int s) {
 }
 
 // Q8_0 word (4 int8). Bias to unsigned (q + 128), place each byte as the low
-// mantissa byte of 2^23, subtract 2^23 + 128: exact q. x stays in natural order.
+// mantissa byte of 2^23, subtract 2^23 + 128: exact q. x is staged in the
+// stored byte order (q8_xorder_elem).
 struct Q8Word { float2 p0, p1; };
 
 __device__ __forceinline__ Q8Word dequant_q8_word(uint32_t w) {

@@ -4,7 +4,9 @@
 // and scale arrays so the kernels read them in contiguous stripes).
 //
 // One thread per block: the block (2 + QB bytes, 2-byte aligned) is read as
-// 16-bit words; the quants are written as 16-byte stores.
+// 16-bit words; in each 16-byte group of quants the two 8-byte halves are
+// interleaved byte by byte (stored byte 2m + h = GGUF byte m + 8h), and the
+// group is written as one 16-byte store.
 #include <cuda_runtime.h>
 
 #include "qg_common.cuh"
@@ -25,7 +27,13 @@ __global__ void repack_kernel(const uint16_t* __restrict__ gguf, size_t nblocks,
 #pragma unroll
     for (int j = 0; j < QB / 4; ++j) w[j] = (uint32_t)src[1 + 2 * j] | ((uint32_t)src[2 + 2 * j] << 16);
 #pragma unroll
-    for (int j = 0; j < QB / 16; ++j) q_out[i * (QB / 16) + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    for (int j = 0; j < QB / 16; ++j) {
+      // GGUF bytes 0-7 of the group are lo = (w0, w1), bytes 8-15 hi = (w2, w3)
+      const uint32_t l0 = w[4 * j], l1 = w[4 * j + 1], h0 = w[4 * j + 2], h1 = w[4 * j + 3];
+      q_out[i * (QB / 16) + j] =
+          make_uint4(__byte_perm(l0, h0, 0x5140), __byte_perm(l0, h0, 0x7362),
+                     __byte_perm(l1, h1, 0x5140), __byte_perm(l1, h1, 0x7362));
+    }
   }
 }
 

@@ -9,16 +9,19 @@
 //
 // GB300 design. A CTA owns 64 rows (4 m-tiles of 16) and a contiguous K range;
 // the CTAs that split K for the same rows form a thread-block cluster.
-//  * One producer warp streams the packed weights and f16 scales of the CTA's
-//    K range with 2-D TMA tiles (128-byte swizzle) into a ring of shared-memory
-//    stages guarded by mbarriers; the tiles stay packed in shared memory.
+//  * One producer warp streams the packed weights, the f16 scales and the f16
+//    activations of the CTA's K range with TMA tiles (128-byte swizzle) into a
+//    ring of shared-memory stages guarded by mbarriers; the weight tiles stay
+//    packed in shared memory.
 //  * Eight consumer warps (4 m-tiles x 2 k-groups) pull the nibble (or int8)
 //    words with ldmatrix straight into the A-fragment layout of
-//    mma.sync.m16n8k16, dequantise them exactly to f16 in registers ((q-8) and
-//    q are exact in f16), and multiply with the f16 activations (B fragments,
-//    pre-permuted once per CTA so the k order matches the dequantised pairs).
-//    Each 32-weight block's product is scaled by its f16 scale in f32, so the
-//    only roundings are the f32 accumulations.
+//    mma.sync.m16n8k16 and dequantise them exactly to f16 in registers ((q-8)
+//    and q are exact in f16). The stored byte order of the blocks (the two
+//    8-byte halves of each 16-byte group interleaved) makes the dequantised
+//    pairs come out in the natural k order of the fragment, so the B fragments
+//    are plain ldmatrix loads of the activation tile. Each 32-weight block's
+//    product is scaled by its f16 scale in f32, so the only roundings are the
+//    f32 accumulations.
 //  * The two k-groups are summed in a fixed order through shared memory, then
 //    the cluster's CTAs are summed in rank order through distributed shared
 //    memory by the rank-0 CTA, which runs the epilogue (y = y0 + acc, or
@@ -39,9 +42,8 @@ namespace qg {
 constexpr int TC_BM = 64;                 // rows per CTA
 constexpr int TC_KT = 256;                // weights per stage (one K unit)
 constexpr int TC_CONSUMERS = 8;           // 4 m-tiles x 2 k-groups
-constexpr int TC_WARP_TMA = TC_CONSUMERS;     // issues the TMA copies
-constexpr int TC_WARP_XP = TC_CONSUMERS + 1;  // permutes x into B-fragment order
-constexpr int TC_THREADS = (TC_CONSUMERS + 2) * 32;
+constexpr int TC_WARP_TMA = TC_CONSUMERS;  // issues the TMA copies
+constexpr int TC_THREADS = (TC_CONSUMERS + 1) * 32;
 constexpr int TC_SMEM_BUDGET = 112 * 1024;  // two CTAs per SM
 constexpr long long TC_WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before giving up
 
@@ -145,10 +147,10 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) 
 }
 
 // ------------------------------------------------------ exact f16 dequant
-// Q4_0: word w = bytes 4t..4t+3 of one row of a block (byte j holds element j
-// low, j+16 high). 0x6400 is f16 1024 (one mantissa step = 1). Results:
-//   e0 = (el 4t, 4t+2), e1 = (4t+16, 4t+18), e2 = (4t+1, 4t+3), e3 = (4t+17, 4t+19)
-// each equal to (q - 8), exactly.
+// Q4_0: word w = stored bytes 4t..4t+3 of one row of a block, i.e. GGUF bytes
+// 2t, 2t+8, 2t+1, 2t+9 (GGUF byte j holds element j low, j+16 high). 0x6400 is
+// f16 1024 (one mantissa step = 1). Results, each equal to (q - 8) exactly:
+//   e0 = (el 2t, 2t+1), e2 = (2t+8, 2t+9), e1 = (2t+16, 2t+17), e3 = (2t+24, 2t+25)
 __device__ __forceinline__ void dq4_f16(uint32_t w, uint32_t& e0, uint32_t& e1, uint32_t& e2,
                                         uint32_t& e3) {
   const uint32_t w8 = w >> 8;
@@ -161,8 +163,8 @@ __device__ __forceinline__ void dq4_f16(uint32_t w, uint32_t& e0, uint32_t& e1, 
   e1 = hfma2_u(and_or<0x00F000F0u>(w, M), k16th, km72);   // (1024 + 16 q) / 16 - 72 = q - 8
   e3 = hfma2_u(and_or<0x00F000F0u>(w8, M), k16th, km72);
 }
-// Q8_0: word w = int8 elements 4t..4t+3 of a 16-element half block:
-//   p0 = (el 4t, 4t+2), p1 = (4t+1, 4t+3), exactly q.
+// Q8_0: word w = stored bytes 4t..4t+3 of a 16-element half block, i.e. its
+// elements 2t, 2t+8, 2t+1, 2t+9:  p0 = (el 2t, 2t+1), p1 = (2t+8, 2t+9), exactly q.
 __device__ __forceinline__ void dq8_f16(uint32_t w, uint32_t& p0, uint32_t& p1) {
   const uint32_t u = w ^ 0x80808080u;          // q + 128
   const uint32_t k1152 = 0x64806480u;          // 1024 + 128
@@ -190,9 +192,8 @@ struct TcShape {
   static constexpr int S_BYTES = TC_BM * 16;             // 8 f16 scales per row per unit
   static constexpr int AS_BYTES = NMAT * (A_BYTES + S_BYTES);  // weights of one unit (TMA)
   static constexpr int CPAD = 8 * NT;
-  static constexpr int X_BYTES = CPAD * TC_KT * 2;       // raw x of one unit (TMA), [4][CPAD][64] f16
-  static constexpr int B_BYTES = 8 * CPAD * 64;          // x of one unit in B-fragment order
-  static constexpr int STAGE = AS_BYTES + X_BYTES + B_BYTES;
+  static constexpr int X_BYTES = CPAD * TC_KT * 2;       // x of one unit (TMA), [4][CPAD][64] f16
+  static constexpr int STAGE = AS_BYTES + X_BYTES;
   static constexpr int NF = 4 * NT * NMAT;               // accumulator floats per lane
   static constexpr int SLOT = 4 * 32 * NF * 4;           // one CTA's partial tile
 };
@@ -208,9 +209,8 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
                                              ~(uintptr_t)1023);
   const int ns = p.ns;
   uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ns * S::STAGE);  // A, S, B ready
-  uint64_t* xfull = full + ns;                                                 // raw x landed
-  uint64_t* empty = xfull + ns;                                                // stage free
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ns * S::STAGE);  // A, S, x landed
+  uint64_t* empty = full + ns;                                                 // stage free
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = blockIdx.x % p.ksplit;
@@ -220,21 +220,18 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   const int u1 = (int)((long)(rank + 1) * p.units / p.ksplit);
   const int nu = u1 - u0;
 
-  // Stage layout: [A, S (weights, TMA)] [raw x (TMA)] [x in B-fragment order].
-  // full[s]: TMA bytes of A and S plus one arrival of the x-permuting warp;
-  // xfull[s]: TMA bytes of raw x; empty[s]: the 8 consumers and the x warp.
+  // Stage layout: [A, S (weights)] [x: 4 boxes of [CPAD][64] f16, 128-byte
+  // swizzle]. full[s]: the TMA bytes of the stage; empty[s]: the 8 consumers.
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) {
-      mbar_init(&full[s], 2);
-      mbar_init(&xfull[s], 1);
-      mbar_init(&empty[s], TC_CONSUMERS + 1);
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], TC_CONSUMERS);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
   const bool producer = warp == TC_WARP_TMA;
-  const bool xwarp = warp == TC_WARP_XP;
   if (producer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
@@ -243,15 +240,13 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         if (i >= ns && !mbar_wait(&empty[s], (uint32_t)(ph ^ 1))) break;
         uint8_t* st = stages + (size_t)s * S::STAGE;
         const int u = u0 + i;
-        mbar_expect_tx(&xfull[s], (uint32_t)S::X_BYTES);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          asm volatile(
-              "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-              " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(st + S::AS_BYTES + q * S::CPAD * 128)),
-              "l"(&mX), "r"(u * TC_KT + q * 64), "r"(0), "r"(smem_u32(&xfull[s]))
-              : "memory");
-        mbar_expect_tx(&full[s], (uint32_t)S::AS_BYTES);
+        mbar_expect_tx(&full[s], (uint32_t)(S::AS_BYTES + S::X_BYTES));
+        // x[0..CPAD)[u*256 .. u*256+256) as [4][CPAD][64] (3-D map, see tc_launch)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(st + S::AS_BYTES)),
+            "l"(&mX), "r"(0), "r"(0), "r"(u * 4), "r"(smem_u32(&full[s]))
+            : "memory");
 #pragma unroll
         for (int m = 0; m < S::NMAT; ++m) {
           const CUtensorMap* mA = m == 0 ? &mA0 : &mA1;
@@ -262,48 +257,6 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
             tma_load_2d(a + bx * TC_BM * 128, mA, u * S::QROW + bx * 128, m0, &full[s], pol_w);
           tma_load_2d(st + S::NMAT * S::A_BYTES + m * S::S_BYTES, mS, u * 8, m0, &full[s], pol_w);
         }
-      }
-    }
-    __syncwarp();
-  } else if (xwarp) {
-    // Permute each unit's raw x into B-fragment order: for block b, column c,
-    // lane slot t, the 16 bytes [x4t, x4t+2, x4t+1, x4t+3, x4t+16, x4t+18,
-    // x4t+17, x4t+19] of that block (columns >= ncols arrive as zeros). Raw x
-    // lands as four [CPAD][64] boxes with the 128-byte swizzle (16-byte chunk q
-    // of row c at chunk q ^ (c & 7)), and slot t of (b, c) is stored at
-    // position (t + (c >> 1)) & 3: both make this warp's loads and stores, and
-    // the consumers' fragment loads, free of bank conflicts.
-    for (int i = 0, s = 0, ph = 0; i < nu; ++i, s = s + 1 == ns ? 0 : s + 1, ph ^= s == 0) {
-      if (!mbar_wait(&xfull[s], (uint32_t)ph)) break;
-      const uint8_t* xr = stages + (size_t)s * S::STAGE + S::AS_BYTES;
-      uint8_t* xb = stages + (size_t)s * S::STAGE + S::AS_BYTES + S::X_BYTES;
-#pragma unroll
-      for (int r = 0; r < (8 * S::CPAD) / 32; ++r) {
-        const int it = lane + 32 * r;
-        const int c = it & (S::CPAD - 1), b = it / S::CPAD;
-        const uint8_t* row = xr + (b >> 1) * (S::CPAD * 128) + c * 128;
-        const int q0i = (b & 1) * 4;
-        const uint4 q0 = *reinterpret_cast<const uint4*>(row + (((q0i + 0) ^ (c & 7)) << 4));
-        const uint4 q1 = *reinterpret_cast<const uint4*>(row + (((q0i + 1) ^ (c & 7)) << 4));
-        const uint4 q2 = *reinterpret_cast<const uint4*>(row + (((q0i + 2) ^ (c & 7)) << 4));
-        const uint4 q3 = *reinterpret_cast<const uint4*>(row + (((q0i + 3) ^ (c & 7)) << 4));
-        const uint32_t lo[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        const uint32_t hi[8] = {q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
-        uint8_t* dst = xb + (b * S::CPAD + c) * 64;
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          *reinterpret_cast<uint4*>(dst + (((t + (c >> 1)) & 3) << 4)) =
-              make_uint4(__byte_perm(lo[2 * t], lo[2 * t + 1], 0x5410),
-                         __byte_perm(lo[2 * t], lo[2 * t + 1], 0x7632),
-                         __byte_perm(hi[2 * t], hi[2 * t + 1], 0x5410),
-                         __byte_perm(hi[2 * t], hi[2 * t + 1], 0x7632));
-      }
-      // raw x was read through the generic proxy and is refilled by TMA
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&full[s]);
-        mbar_arrive(&empty[s]);
       }
     }
     __syncwarp();
@@ -319,7 +272,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[m][n][e] = 0.f;
 
-  if (!producer && !xwarp) {
+  if (!producer) {
     // k-group kj owns the four contiguous blocks 4kj..4kj+3 of every unit.
     // ldmatrix source of this lane: lanes 0-7 rows 0-7 and lanes 8-15 rows 8-15
     // of the m-tile at chunk c; lanes 16-31 the same rows at chunk c+1. The
@@ -336,8 +289,13 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     }
     const uint32_t soff_g = (uint32_t)((mi * 16 + g) * 16 + 8 * kj);
     const uint32_t soff_g8 = (uint32_t)((mi * 16 + g + 8) * 16 + 8 * kj);
-    const uint32_t boff =
-        (uint32_t)(S::AS_BYTES + S::X_BYTES + ((4 * kj * S::CPAD + g) * 4 + ((t + (g >> 1)) & 3)) * 16);
+    // B fragments: ldmatrix.x4 of x rows (columns) n*8 + (lane & 7) at the k
+    // offsets 0, 8, 16, 24 of a block (matrix lane >> 3). Block 4kj + j of the
+    // unit lies in x box 2kj + (j >> 1) at 16-byte chunk 4(j & 1) + (lane >> 3),
+    // stored at chunk ^ row (the 128-byte swizzle; rows are 128 bytes).
+    const int lm = lane >> 3, lr = lane & 7;
+    const uint32_t boff = (uint32_t)(S::AS_BYTES + 2 * kj * S::CPAD * 128 + lr * 128);
+    const uint32_t xo0 = (uint32_t)((lm ^ lr) << 4), xo1 = (uint32_t)(((4 + lm) ^ lr) << 4);
     for (int i = 0, s = 0, ph = 0; i < nu; ++i, s = s + 1 == ns ? 0 : s + 1, ph ^= s == 0) {
       if (!mbar_wait(&full[s], (uint32_t)ph)) break;
       const uint32_t st = smem_u32(stages + (size_t)s * S::STAGE);
@@ -371,7 +329,9 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 #pragma unroll
       for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int n = 0; n < NT; ++n) bf[j][n] = lds128(bbase + (uint32_t)((j * S::CPAD + n * 8) * 64));
+        for (int n = 0; n < NT; ++n)
+          ldsm_x4(bbase + (uint32_t)((j >> 1) * S::CPAD * 128 + n * 1024) + ((j & 1) ? xo1 : xo0),
+                  bf[j][n].x, bf[j][n].y, bf[j][n].z, bf[j][n].w);
       // Then the blocks in groups of JB, so that every group carries four
       // independent mma chains whatever the tile shape.
       constexpr int JB = 4 / (S::NMAT * NT) > 0 ? 4 / (S::NMAT * NT) : 1;
@@ -440,7 +400,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 
   // ---- reduce the two k-groups (fixed order: kj 0 + kj 1) in shared memory
   float* scratch = reinterpret_cast<float*>(stages);
-  if (!producer && !xwarp) {
+  if (!producer) {
     asm volatile("bar.sync 1, %0;" ::"n"(TC_CONSUMERS * 32) : "memory");
     if (kj == 1) {
       float* dst = scratch + (size_t)(mi * 32 + lane) * S::NF;
@@ -468,7 +428,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   // ---- reduce the cluster's K splits in rank order through distributed smem
   if (p.ksplit > 1) {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (!producer && !xwarp && kj == 0 && rank != 0) {
+    if (!producer && kj == 0 && rank != 0) {
       const uint32_t local = smem_u32(stages) +
                              (uint32_t)(((rank - 1) * 4 * 32 + mi * 32 + lane) * S::NF * 4);
       uint32_t remote;
@@ -486,7 +446,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
           }
     }
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (!producer && !xwarp && kj == 0 && rank == 0) {
+    if (!producer && kj == 0 && rank == 0) {
       for (int r = 1; r < p.ksplit; ++r) {
         const float* srcp = scratch + (size_t)(((r - 1) * 4 * 32) + mi * 32 + lane) * S::NF;
         int q = 0;
@@ -501,7 +461,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   }
 
   // ---- epilogue (rank 0, k-group 0)
-  if (producer || xwarp || kj != 0 || rank != 0) return;
+  if (producer || kj != 0 || rank != 0) return;
 #pragma unroll
   for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -559,30 +519,32 @@ struct TcConfig {
 
 // Pinned per shape: depends only on (type, columns, dual, rows, k), never on
 // the device, so the reduction order is the same on every GPU. The K split is
-// the largest that keeps every CTA in one wave of a fixed 304-CTA capacity
-// (two per SM on a 152-SM part): each CTA then streams as much K as possible,
-// which amortises its start-up and reduction. Stages: as many as fit, up to
-// the CTA's whole K range.
+// the largest (at most 8) whose clusters all fit in one wave of a GB300: the
+// tables hold, per cluster size, how many clusters the part keeps resident at
+// once (measured with cudaOccupancyMaxActiveClusters for these kernels; two
+// CTAs per SM, or one for the large-stage plan). Each CTA then streams as much
+// K as possible, which amortises its start-up and reduction. Stages: as many
+// as fit, up to the CTA's whole K range.
+constexpr int kClusterCap2[9] = {0, 304, 152, 97, 74, 58, 46, 38, 36};  // 2 CTAs / SM
+constexpr int kClusterCap1[9] = {0, 152, 76, 46, 36, 28, 23, 15, 15};   // 1 CTA / SM
+
 template <int QT, int NT, bool DUAL>
-TcConfig pick_config_budget(int rows, int k, size_t budget) {
+TcConfig pick_config_budget(int rows, int k, size_t budget, const int (&cap)[9]) {
   using S = TcShape<QT, NT, DUAL>;
   const int units = k / TC_KT;
   const int ntile = (rows + TC_BM - 1) / TC_BM;
-  const int capacity = 304;
-  int ks = capacity / ntile;
-  if (ks > 8) ks = 8;
-  if (ks > units) ks = units;
-  if (ks < 1) ks = 1;
+  int ks = 8;
+  while (ks > 1 && (ks > units || ntile > cap[ks])) --ks;
   for (; ks >= 1; --ks) {
     const int nu_max = (units + ks - 1) / ks;
-    int ns = (int)((budget - 1024) / (S::STAGE + 3 * sizeof(uint64_t)));
+    int ns = (int)((budget - 1024) / (S::STAGE + 2 * sizeof(uint64_t)));
     if (ns > 8) ns = 8;
     if (ns > nu_max) ns = nu_max;
     if (ns < 2 && nu_max >= 2) continue;
     if (ns < 1) continue;
     const size_t reuse = (size_t)ns * S::STAGE;
     if ((size_t)S::SLOT > reuse || (size_t)(ks - 1) * S::SLOT > reuse) continue;
-    return TcConfig{ks, ns, 1024 + reuse + 3 * ns * sizeof(uint64_t)};
+    return TcConfig{ks, ns, 1024 + reuse + 2 * ns * sizeof(uint64_t)};
   }
   return TcConfig{0, 0, 0};
 }
@@ -590,8 +552,8 @@ TcConfig pick_config_budget(int rows, int k, size_t budget) {
 // Two CTAs per SM when the shape allows it, else one.
 template <int QT, int NT, bool DUAL>
 TcConfig pick_config(int rows, int k) {
-  TcConfig c = pick_config_budget<QT, NT, DUAL>(rows, k, TC_SMEM_BUDGET);
-  if (c.ksplit == 0) c = pick_config_budget<QT, NT, DUAL>(rows, k, 220 * 1024);
+  TcConfig c = pick_config_budget<QT, NT, DUAL>(rows, k, TC_SMEM_BUDGET, kClusterCap2);
+  if (c.ksplit == 0) c = pick_config_budget<QT, NT, DUAL>(rows, k, 220 * 1024, kClusterCap1);
   return c;
 }
 
@@ -622,12 +584,22 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
     mA1 = mA0;
     mS1 = mS0;
   }
-  // x as a [ncols][k] f16 tensor; boxes of [CPAD rows][64 columns] with the
-  // 128-byte swizzle, rows past ncols read as zero
+  // x as a 3-D view of the [ncols][k] f16 array: {64 elements, column, k/64},
+  // strides 2k and 128 bytes, so one box {64, CPAD, 4} brings a unit's 256 k as
+  // four [CPAD][64] tiles (128-byte swizzle); columns past ncols read as zero.
   CUtensorMap mX;
-  if (!make_map(&mX, x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)k, (uint64_t)ncols, 64,
-                S::CPAD, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  {
+    auto enc = get_encode();
+    if (!enc) return cudaErrorInvalidValue;
+    cuuint64_t dims[3] = {64, (cuuint64_t)ncols, (cuuint64_t)k / 64};
+    cuuint64_t strides[2] = {(cuuint64_t)k * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)S::CPAD, 4};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&mX, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(x), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   TcParams p{};
   p.rows = rows;
   p.k = k;

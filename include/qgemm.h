@@ -11,9 +11,15 @@
  * repacked at load time into separate nibble and scale arrays so that kernels
  * read contiguous stripes). A matrix W of `rows` x `k` weights (k a multiple of
  * 32) is passed as two row-major device arrays:
- *   quants: Q4_0 uint8 [rows][k/2]  (16 bytes per block, in-block order as GGUF)
- *           Q8_0 int8  [rows][k]
+ *   quants: Q4_0 uint8 [rows][k/2]  (16 bytes per block)
+ *           Q8_0 int8  [rows][k]    (32 bytes per block)
  *   scales: uint16 [rows][k/32]      (f16 bit patterns)
+ * In-block byte order: a block's quant bytes are taken in 16-byte groups (one
+ * group for Q4_0, two for Q8_0), and in each group the two 8-byte halves are
+ * interleaved byte by byte: stored byte 2m + h is GGUF byte m + 8h of the group
+ * (m = 0..7, h = 0..1). qrepack produces this order from GGUF blocks. It lets
+ * a tensor-core fragment load hand each lane the bytes of elements 2t, 2t+1,
+ * 2t+8, 2t+9 together, so the activations need no reordering on that path.
  * Activations X are f16 [ncols][k] (column c is the c-th input vector), outputs
  * Y are f32 [ncols][rows].
  *

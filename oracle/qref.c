@@ -346,7 +346,10 @@ int qref_moe(int type, const void *qg, const uint16_t *sg, const void *qu,
 
 /* GGUF interleaved blocks (per block: f16 d little endian, then the quant
  * bytes) -> separate quant array [rows][k/32 * qbytes] and scale array
- * [rows][k/32]. */
+ * [rows][k/32]. The stored quant order is the library's: in every 16-byte
+ * group of a block's quants, stored byte 2m + h is GGUF byte m + 8h
+ * (m = 0..7, h = 0..1), i.e. the two 8-byte halves interleaved byte by byte.
+ * Test infrastructure: this is the oracle's statement of that layout. */
 int qref_repack(int type, const uint8_t *gguf, int rows, int k, uint8_t *q_out,
                 uint16_t *scl_out) {
   int qb = qbytes_per_block(type);
@@ -357,7 +360,10 @@ int qref_repack(int type, const uint8_t *gguf, int rows, int k, uint8_t *q_out,
     for (int b = 0; b < nb; ++b) {
       const uint8_t *blk = gguf + ((size_t)r * nb + b) * (size_t)(2 + qb);
       scl_out[(size_t)r * nb + b] = (uint16_t)(blk[0] | (blk[1] << 8));
-      memcpy(q_out + ((size_t)r * nb + b) * (size_t)qb, blk + 2, (size_t)qb);
+      uint8_t *dst = q_out + ((size_t)r * nb + b) * (size_t)qb;
+      for (int g = 0; g < qb; g += 16)
+        for (int m = 0; m < 8; ++m)
+          for (int h = 0; h < 2; ++h) dst[g + 2 * m + h] = blk[2 + g + m + 8 * h];
     }
   }
   return 0;

@@ -6,17 +6,22 @@ the kernels and the oracle read. It performs none of the method's arithmetic
 the CUDA path and the CPU oracle without linking them.
 
 Storage formats (the block format of "Engine and kernels", pooled.run, section
-"What it runs": 32 weights plus one f16 scale per block; the load-time repack of
-"Architecture", section "Memory and caching", into separate nibble and scale
-arrays):
+"What it runs": 32 weights plus one f16 scale per block):
 
-* Q4_0, repacked: ``nib`` uint8 ``[rows, k/2]`` (16 bytes per 32-weight block;
-  byte j of a block holds element j in its low nibble and element j+16 in its
-  high nibble) and ``scl`` uint16 ``[rows, k/32]`` (f16 bit patterns).
-* Q8_0, repacked: ``qs`` int8 ``[rows, k]`` and ``scl`` uint16 ``[rows, k/32]``.
-* GGUF interleaved blocks (the input of the repack step): per block the f16
-  scale ``d`` (2 bytes, little endian) followed by the 16 (Q4_0) or 32 (Q8_0)
-  quant bytes; blocks of a row are consecutive, rows are consecutive.
+* Q4_0, split: ``nib`` uint8 ``[rows, k/2]`` (16 bytes per 32-weight block, in
+  GGUF in-block order: byte j of a block holds element j in its low nibble and
+  element j+16 in its high nibble) and ``scl`` uint16 ``[rows, k/32]`` (f16 bit
+  patterns).
+* Q8_0, split: ``qs`` int8 ``[rows, k]`` (GGUF order) and ``scl`` uint16
+  ``[rows, k/32]``.
+* GGUF interleaved blocks (the input of the load-time repack of
+  "Architecture", section "Memory and caching"): per block the f16 scale ``d``
+  (2 bytes, little endian) followed by the 16 (Q4_0) or 32 (Q8_0) quant bytes;
+  blocks of a row are consecutive, rows are consecutive.
+
+The oracle reads the split arrays. The library reads its own stored layout,
+which the repack (the library's ``qrepack`` or the oracle's ``repack``) makes
+from the GGUF blocks; this module never produces it.
 
 Draw order inside one workload, from one ``numpy.random.Generator(PCG64(seed))``:
 weights q, then scales, then X, then y0, then expert ids, then routing logits.
@@ -47,7 +52,7 @@ def qbytes_per_row(qtype: int, k: int) -> int:
 
 
 def weight_bytes(qtype: int, rows: int, k: int) -> int:
-    """Bytes of one quantised matrix in the repacked layout (quants + f16 scales)."""
+    """Bytes of one quantised matrix (quants + f16 scales)."""
     return rows * (qbytes_per_row(qtype, k) + (k // QK) * 2)
 
 
@@ -93,7 +98,7 @@ def draw_routing(g: np.random.Generator, ncols: int, n_expert: int, topk: int):
 
 
 def to_gguf_blocks(qtype: int, q: np.ndarray, scl: np.ndarray) -> np.ndarray:
-    """Interleave repacked arrays into GGUF blocks: per block d then the quants."""
+    """Interleave split arrays into GGUF blocks: per block d then the quants."""
     rows = q.shape[0]
     nb = scl.shape[1]
     qb = BLOCK_QBYTES[qtype]

@@ -24,6 +24,26 @@ def dev_u16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
 
 
+def kernel_layout(qtype, q, scl):
+    """The library's stored layout of a matrix given as GGUF-order split arrays:
+    the oracle's repack of its GGUF blocks. Stacked expert matrices pass as one
+    tall matrix. Returns (quants, scales)."""
+    import oracle
+    import synth
+    q = np.ascontiguousarray(q)
+    rows, nb = scl.shape[0] if scl.ndim == 2 else scl.shape[0] * scl.shape[1], scl.shape[-1]
+    q2 = q.reshape(rows, -1)
+    s2 = np.ascontiguousarray(scl).reshape(rows, nb)
+    qr, sr = oracle.repack(qtype, synth.to_gguf_blocks(qtype, q2, s2), rows, nb * 32)
+    return qr.reshape(q.shape), sr.reshape(scl.shape)
+
+
+def dev_q(qtype, q, scl):
+    """Device copies (quants, scales) of a GGUF-order matrix in the library's layout."""
+    qr, sr = kernel_layout(qtype, q, scl)
+    return dev(qr), dev_u16(sr)
+
+
 def host(t):
     return t.detach().cpu().numpy()
 

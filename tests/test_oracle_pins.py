@@ -103,6 +103,10 @@ def test_golden_repack(oracle_lib):
     q, s = oracle_lib.repack(synth.Q4_0, np.frombuffer(blk, dtype=np.uint8), 1, 32)
     assert s[0, 0] == int(rp["expected_scale"], 16)
     assert q.tobytes() == bytes.fromhex(rp["expected_nib_hex"])
+    blk = bytes.fromhex(rp["q8_block_hex"].replace(" ", ""))
+    q, s = oracle_lib.repack(synth.Q8_0, np.frombuffer(blk, dtype=np.uint8), 1, 32)
+    assert s[0, 0] == int(rp["expected_q8_scale"], 16)
+    assert q.tobytes() == bytes.fromhex(rp["expected_q8_hex"])
 
 
 def test_f16_decoder_all_patterns(oracle_lib):
@@ -311,14 +315,23 @@ def test_moe_shared_only_and_empty_routing(oracle_lib):
     assert np.all(bound > 0)
 
 
-def test_repack_roundtrip(oracle_lib):
+def test_repack_is_one_group_permutation(oracle_lib):
+    """Scales pass through unchanged, and every 16-byte group of every block of
+    every row is reordered by the same permutation: the one a block of distinct
+    bytes 0..15 reveals (pinned by the golden block above)."""
+    probe = np.concatenate([[0, 0], np.arange(16)]).astype(np.uint8)
+    perm, _ = oracle_lib.repack(synth.Q4_0, probe, 1, 32)
+    perm = perm.view(np.uint8).reshape(16).astype(np.int64)
+    assert sorted(perm.tolist()) == list(range(16))
     for qtype in (synth.Q4_0, synth.Q8_0):
         g = synth.rng(13)
         q, s = synth.draw_matrix(g, qtype, 7, 96)
         blocks = synth.to_gguf_blocks(qtype, q, s)
         q2, s2 = oracle_lib.repack(qtype, blocks, 7, 96)
-        assert np.array_equal(q2.view(np.uint8), q.view(np.uint8))
         assert np.array_equal(s2, s)
+        a = q.view(np.uint8).reshape(7, -1, 16)
+        b = q2.view(np.uint8).reshape(7, -1, 16)
+        assert np.array_equal(b, a[:, :, perm])
 
 
 def test_h_bound_dominates_f16_rounding(oracle_lib):

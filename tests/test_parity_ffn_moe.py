@@ -13,7 +13,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import NTHREADS, assert_within, dev, dev_u16, dev_u16_as_f16, gemv_bound, host
+from helpers import NTHREADS, assert_within, dev, dev_q, dev_u16, dev_u16_as_f16, gemv_bound, host
 
 pytestmark = pytest.mark.gpu
 
@@ -35,7 +35,7 @@ import gemm_q4_q8_gb300 as qg  # noqa: E402
 def gpu_gate_up(qtype, qg_, sg, qu, su, x):
     rows = sg.shape[0]
     h = torch.full((x.shape[0], rows), float("nan"), dtype=torch.float16, device="cuda")
-    qg.qffn_gate_up_silu(qtype, dev(qg_), dev_u16(sg), dev(qu), dev_u16(su), dev_u16_as_f16(x), h)
+    qg.qffn_gate_up_silu(qtype, *dev_q(qtype, qg_, sg), *dev_q(qtype, qu, su), dev_u16_as_f16(x), h)
     torch.cuda.synchronize()
     return host(h.view(torch.int16)).view(np.uint16)
 
@@ -68,7 +68,7 @@ def test_prefill_ffn_16_columns():
     hb, href, g, u, Sg, Su = check_gate_up(c["qtype"], c["qg"], c["sg"], c["qu"], c["su"], c["x"],
                                            "prefill gate/up 17408x5120 C=16")
     y = dev(c["y0"])
-    qg.qgemm_cols(c["qtype"], dev(c["qd"]), dev_u16(c["sd"]), dev_u16_as_f16(hb), y, y)
+    qg.qgemm_cols(c["qtype"], *dev_q(c["qtype"], c["qd"], c["sd"]), dev_u16_as_f16(hb), y, y)
     torch.cuda.synchronize()
     got = host(y)
     # staged: the oracle down-projects the GPU's own h
@@ -94,10 +94,13 @@ def gpu_moe(case, ids=None, with_y0=True, nshared=True):
     uniq = torch.full((ncols * topk,), -7, dtype=torch.int32, device="cuda")
     sh = None
     if case.get("shared") is not None and nshared:
-        sh = {n: (dev_u16(v) if n.startswith("s") else dev(v)) for n, v in case["shared"].items()}
+        s_ = case["shared"]
+        sh = {}
+        for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
+            sh[a], sh[b] = dev_q(t, s_[a], s_[b])
     y0 = dev(case["y0"]) if (case.get("y0") is not None and with_y0) else None
-    qg.qmoe_experts(t, dev(case["qg"]), dev_u16(case["sg"]), dev(case["qu"]), dev_u16(case["su"]),
-                    dev(case["qd"]), dev_u16(case["sd"]), E, ffn, hidden,
+    qg.qmoe_experts(t, *dev_q(t, case["qg"], case["sg"]), *dev_q(t, case["qu"], case["su"]),
+                    *dev_q(t, case["qd"], case["sd"]), E, ffn, hidden,
                     dev(np.ascontiguousarray(ids, np.int32)), dev(case["rw"]),
                     dev_u16_as_f16(case["x"]), y, ws, y0=y0, shared=sh, err_flag=err,
                     uniq_ids_out=uniq)

@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import NTHREADS, assert_within, dev, dev_u16, dev_u16_as_f16, gemv_bound, host
+from helpers import NTHREADS, assert_within, dev, dev_q, dev_u16_as_f16, gemv_bound, host
 
 pytestmark = pytest.mark.gpu
 
@@ -29,8 +29,7 @@ import gemm_q4_q8_gb300 as qg  # noqa: E402
 
 
 def run_gemv(qtype, q, scl, x, y0=None, api="gemv", inplace=False):
-    dq = dev(q)
-    ds = dev_u16(scl)
+    dq, ds = dev_q(qtype, q, scl)
     dx = dev_u16_as_f16(x)
     ncols, rows = x.shape[0], scl.shape[0]
     y = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")

@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import assert_within, dev, dev_u16, dev_u16_as_f16, host
+from helpers import assert_within, dev, dev_q, dev_u16_as_f16, host
 
 torch = pytest.importorskip("torch")
 
@@ -17,12 +17,18 @@ import gemm_q4_q8_gb300 as qg  # noqa: E402
 
 
 def _moe_args(case):
+    t = case["qtype"]
     sh = None
     if case.get("shared") is not None:
-        sh = {n: (dev_u16(v) if n.startswith("s") else dev(v)) for n, v in case["shared"].items()}
+        s_ = case["shared"]
+        sh = {}
+        for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
+            sh[a], sh[b] = dev_q(t, s_[a], s_[b])
     y0 = dev(case["y0"]) if case.get("y0") is not None else None
-    return dict(qg=dev(case["qg"]), sg=dev_u16(case["sg"]), qu=dev(case["qu"]),
-                su=dev_u16(case["su"]), qd=dev(case["qd"]), sd=dev_u16(case["sd"]),
+    dqg, dsg = dev_q(t, case["qg"], case["sg"])
+    dqu, dsu = dev_q(t, case["qu"], case["su"])
+    dqd, dsd = dev_q(t, case["qd"], case["sd"])
+    return dict(qg=dqg, sg=dsg, qu=dqu, su=dsu, qd=dqd, sd=dsd,
                 ids=dev(np.ascontiguousarray(case["ids"], np.int32)), rw=dev(case["rw"]),
                 x=dev_u16_as_f16(case["x"]), y0=y0, shared=sh)
 
