@@ -92,10 +92,16 @@ __device__ __forceinline__ void load_x16(const float* col, int plane, int bi, fl
 // f32 in the consumption order of QT. One thread per 32-element block: its four
 // 16-byte loads are issued before any use, so a CTA pays about one global-load
 // latency per pass instead of one per element.
-__device__ __forceinline__ void stage_block(int qt, float* col, int plane, int bi,
-                                            const __half* src) {
+struct XBlk { uint4 v0, v1, v2, v3; };  // one 32-element f16 block of x
+
+__device__ __forceinline__ XBlk load_xblk(const __half* src) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
-  const uint4 v0 = s4[0], v1 = s4[1], v2 = s4[2], v3 = s4[3];
+  return XBlk{s4[0], s4[1], s4[2], s4[3]};
+}
+
+// Write a loaded x block into the staged layout (see stage_block).
+__device__ __forceinline__ void stage_xblk(int qt, float* col, int plane, int bi, const XBlk& xb) {
+  const uint4 v0 = xb.v0, v1 = xb.v1, v2 = xb.v2, v3 = xb.v3;
   __align__(16) __half h[32];
   *reinterpret_cast<uint4*>(&h[0]) = v0;
   *reinterpret_cast<uint4*>(&h[8]) = v1;
@@ -109,6 +115,11 @@ __device__ __forceinline__ void stage_block(int qt, float* col, int plane, int b
   float4* d4 = reinterpret_cast<float4*>(col) + bi;
 #pragma unroll
   for (int i = 0; i < 8; ++i) d4[i * plane] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+}
+
+__device__ __forceinline__ void stage_block(int qt, float* col, int plane, int bi,
+                                            const __half* src) {
+  stage_xblk(qt, col, plane, bi, load_xblk(src));
 }
 
 // Column c occupies xs[c * xstride ...] (xstride = 32 * plane floats).

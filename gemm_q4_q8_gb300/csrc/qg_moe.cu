@@ -60,20 +60,62 @@ struct MoeDev {
 
 // Stage the selected columns of x (column stride `colstride` halves, k wide)
 // as f32 in the consumption order of qt, one 32-element block per thread.
+// Two blocks per thread per pass, both loads issued before either is written.
 __device__ __forceinline__ void stage_x_cols(int qt, float* xs, int xstride, const __half* x,
                                              size_t colstride, int ncols, int k) {
   const int nbk = k / QK;
-  for (int it = threadIdx.x; it < ncols * nbk; it += blockDim.x) {
+  const int total = ncols * nbk;
+  for (int it = threadIdx.x; it < total; it += 2 * blockDim.x) {
+    const int it2 = it + blockDim.x;
     const int c = it / nbk, b = it % nbk;
-    stage_block(qt, xs + c * xstride, xstride / QK, b, x + (size_t)c * colstride + (size_t)b * QK);
+    const XBlk a = load_xblk(x + (size_t)c * colstride + (size_t)b * QK);
+    XBlk a2;
+    const int c2 = it2 / nbk, b2 = it2 % nbk;
+    if (it2 < total) a2 = load_xblk(x + (size_t)c2 * colstride + (size_t)b2 * QK);
+    stage_xblk(qt, xs + c * xstride, xstride / QK, b, a);
+    if (it2 < total) stage_xblk(qt, xs + c2 * xstride, xstride / QK, b2, a2);
   }
 }
 
 // ------------------------------------------------------------ K1: gate/up
+// The MOE_RW1 rows of one work item: pair pp (expert slice or shared expert,
+// column c, k slot j), rows r0 .. r0 + MOE_RW1 - 1 (clamped reads past ffn).
+template <int QT>
+struct MoeK1Rows {
+  const uint8_t *qa, *qb;
+  const uint16_t *sa, *sb;
+  int c, j, r0;
+  int row[MOE_RW1];
+};
+
+template <int QT>
+__device__ __forceinline__ MoeK1Rows<QT> moe_k1_rows(const MoeDev& p, const int16_t* s_order,
+                                                     const int* s_ids, const int8_t* s_pc,
+                                                     const int8_t* s_pj, int n, int pp, int g,
+                                                     size_t mat_q, size_t mat_s) {
+  MoeK1Rows<QT> w;
+  const int code = s_order[pp];
+  w.c = s_pc[pp];
+  w.j = s_pj[pp];
+  if (code < n) {
+    const size_t e = (size_t)s_ids[code];
+    w.qa = p.qg + e * mat_q; w.sa = p.sg + e * mat_s;
+    w.qb = p.qu + e * mat_q; w.sb = p.su + e * mat_s;
+  } else {
+    w.qa = p.sqg; w.sa = p.ssg; w.qb = p.squ; w.sb = p.ssu;
+  }
+  w.r0 = g * MOE_RW1;
+#pragma unroll
+  for (int r = 0; r < MOE_RW1; ++r) w.row[r] = min(w.r0 + r, p.ffn - 1);
+  return w;
+}
+
 template <int QT>
 __global__ void __launch_bounds__(MOE_THREADS, 2) moe_gate_up_kernel(const MoeDev p) {
   __shared__ int s_ids[MOE_MAXN];
+  __shared__ __align__(16) int s_key[MOE_MAXN];   // id * 128 + position, or INT_MAX
   __shared__ int16_t s_order[MOE_MAXN + 8];
+  __shared__ int8_t s_pc[MOE_MAXN + 8], s_pj[MOE_MAXN + 8];  // column and k slot of each pair
   extern __shared__ float4 smem_f4[];
   float* xs = reinterpret_cast<float*>(smem_f4);
   constexpr int QB = QTraits<QT>::QB;
@@ -89,16 +131,27 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_gate_up_kernel(const MoeDe
     valid = id >= 0 && id < p.n_expert;
     s_ids[t] = valid ? id : -1;
   }
+  if (t < MOE_MAXN) s_key[t] = valid ? id * MOE_MAXN + t : 0x7fffffff;
   const int nvalid = __syncthreads_count(valid);
   if (valid) {
+    // rank = number of keys below this one (keys are distinct)
+    const int key = id * MOE_MAXN + t;
+    const int4* k4 = reinterpret_cast<const int4*>(s_key);
     int rank = 0;
-    for (int s = 0; s < n; ++s) {
-      const int o = s_ids[s];
-      rank += (o >= 0 && (o < id || (o == id && s < t))) ? 1 : 0;
+#pragma unroll 4
+    for (int s = 0; s < (n + 3) / 4; ++s) {
+      const int4 o = k4[s];
+      rank += (o.x < key) + (o.y < key) + (o.z < key) + (o.w < key);
     }
     s_order[rank] = (int16_t)t;
+    s_pc[rank] = (int8_t)(t / p.topk);
+    s_pj[rank] = (int8_t)(t % p.topk);
   }
-  if (p.has_shared && t < p.ncols) s_order[nvalid + t] = (int16_t)(n + t);
+  if (p.has_shared && t < p.ncols) {
+    s_order[nvalid + t] = (int16_t)(n + t);
+    s_pc[nvalid + t] = (int8_t)t;
+    s_pj[nvalid + t] = (int8_t)p.topk;
+  }
   __syncthreads();
   const int P = nvalid + (p.has_shared ? p.ncols : 0);
 
@@ -123,50 +176,35 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_gate_up_kernel(const MoeDe
   }
 
   const int k = p.hidden;
-  stage_x_cols(QT, xs, k, p.x, (size_t)k, p.ncols, k);
-  __syncthreads();
-
   const int lane = t & 31, warp = t >> 5;
   const int nb = k / QK;
   const size_t rowbytes = (size_t)nb * QB;
   const size_t mat_q = (size_t)p.ffn * rowbytes;
   const size_t mat_s = (size_t)p.ffn * nb;
   const int ngroups = (p.ffn + MOE_RW1 - 1) / MOE_RW1;
-  const long total = (long)P * ngroups;
-  for (long item = (long)blockIdx.x * MOE_WARPS + warp; item < total;
-       item += (long)gridDim.x * MOE_WARPS) {
-    const int pp = (int)(item / ngroups), g = (int)(item % ngroups);
-    const int code = s_order[pp];
-    int c, j;
-    const uint8_t *qa, *qb;
-    const uint16_t *sa, *sb;
-    if (code < n) {
-      c = code / p.topk;
-      j = code % p.topk;
-      const size_t e = (size_t)s_ids[code];
-      qa = p.qg + e * mat_q; sa = p.sg + e * mat_s;
-      qb = p.qu + e * mat_q; sb = p.su + e * mat_s;
-    } else {
-      c = code - n;
-      j = p.topk;
-      qa = p.sqg; sa = p.ssg; qb = p.squ; sb = p.ssu;
-    }
-    const int r0 = g * MOE_RW1;
-    int rowidx[MOE_RW1];
-#pragma unroll
-    for (int r = 0; r < MOE_RW1; ++r) rowidx[r] = min(r0 + r, p.ffn - 1);
+  const int total = P * ngroups;
+  const int stride = gridDim.x * MOE_WARPS;
+  int item = blockIdx.x * MOE_WARPS + warp;
+
+  stage_x_cols(QT, xs, k, p.x, (size_t)k, p.ncols, k);
+  __syncthreads();
+
+  for (; item < total; item += stride) {
+    const MoeK1Rows<QT> cur = moe_k1_rows<QT>(p, s_order, s_ids, s_pc, s_pj, n, item / ngroups,
+                                              item % ngroups, mat_q, mat_s);
     float ta[MOE_RW1], tb[MOE_RW1];
 #pragma unroll
     for (int r = 0; r < MOE_RW1; ++r) { ta[r] = 0.f; tb[r] = 0.f; }
-    cc_rowdot_1col<QT, MOE_RW1, true>(qa, sa, qb, sb, rowbytes, nb, rowidx, xs + c * k, nb, 0, nb,
-                                      lane, ta, tb);
+    cc_rowdot_1col<QT, MOE_RW1, true>(cur.qa, cur.sa, cur.qb, cur.sb, rowbytes, nb, cur.row,
+                                      xs + cur.c * k, nb, 0, nb, lane, ta, tb);
     int idx, idx2;
     const float gs = warp_transpose_reduce<MOE_RW1>(ta, lane, idx);
     const float us = warp_transpose_reduce<MOE_RW1>(tb, lane, idx2);
     if ((lane & (32 / MOE_RW1 - 1)) == 0) {
-      const int row = r0 + idx;
+      const int row = cur.r0 + idx;
       if (row < p.ffn)
-        p.hws[((size_t)c * (p.topk + 1) + j) * p.ffn + row] = __float2half_rn(silu_f32(gs) * us);
+        p.hws[((size_t)cur.c * (p.topk + 1) + cur.j) * p.ffn + row] =
+            __float2half_rn(silu_f32(gs) * us);
     }
   }
 }
