@@ -81,6 +81,24 @@ qmv_cc_kernel(const CCParams p) {
   const int gfirst = blockIdx.x * CC_WARPS;
   const int iters = gfirst < ngroups ? (ngroups - gfirst + gstride - 1) / gstride : 0;
 
+  pdl_trigger();
+  // The first 32 blocks of every row of this CTA's first row groups are pulled
+  // into L2 before waiting for the previous kernel (weights are never written
+  // by it), so the stream starts while that kernel drains and x is staged.
+  if (nchunk == 1 && iters > 0 && threadIdx.x < CC_WARPS * RW) {
+    const int row = gfirst * RW + (int)threadIdx.x;
+    if (row < p.rows) {
+      const int pb = (nb < 32 ? nb : 32) * QB;
+      l2_prefetch_bulk(p.qa + (size_t)row * rowbytes, (uint32_t)pb);
+      l2_prefetch_line(p.sa + (size_t)row * nb);
+      if (DUAL) {
+        l2_prefetch_bulk(p.qb + (size_t)row * rowbytes, (uint32_t)pb);
+        l2_prefetch_line(p.sb + (size_t)row * nb);
+      }
+    }
+  }
+  pdl_wait();
+
   if (nchunk == 1) {
     stage_x<QT, NC>(xs, xstride, p.x, k, cols, 0, nb);
     __syncthreads();
@@ -208,10 +226,8 @@ static cudaError_t launch_cc_t(const CCParams& p0, cudaStream_t s, int* nlaunch)
   const long maxgrid = (long)device_sm_count() * occ;
   if (grid > maxgrid) grid = maxgrid;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, CC_THREADS, smem, s>>>(p);
-  note_launch();
   if (nlaunch) ++*nlaunch;
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(CC_THREADS), smem, s, 0, p);
 }
 
 template <int QT, bool DUAL, int EPI>

@@ -152,6 +152,28 @@ __device__ __forceinline__ Q8Word dequant_q8_word(uint32_t w) {
   return r;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Kernels of this library are launched with programmatic stream
+// serialisation: a kernel may start while the previous kernel on the stream is
+// finishing. pdl_trigger() lets the next kernel start early (the CUDA-core
+// kernels call it at their start; the tensor-core kernel never does, see
+// qg_tc.cu); pdl_wait() blocks
+// until every earlier kernel on the stream has completed and its writes are
+// visible. Each kernel reads only weights (immutable inputs) before pdl_wait()
+// and touches activations, residuals, ids and outputs only after it. Launched
+// without the attribute, both instructions are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// L2 prefetch hints: a 16-byte aligned range whose size is a multiple of 16
+// (bulk), or the cache line holding one address.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void l2_prefetch_line(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // --------------------------------------------------- warp reductions
 // Reduce N values (N a power of two, 1..32) over the 32 lanes of a warp so that
 // each value's total ends up in some lane; returns the total held by this lane

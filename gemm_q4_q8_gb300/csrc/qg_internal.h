@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "qgemm.h"
 
 namespace qg {
@@ -15,6 +17,36 @@ int device_sm_count();
 
 // Count one kernel launch (see qg_kernel_launches).
 void note_launch(int n = 1);
+
+// Launch `kern` with programmatic stream serialisation (the kernel may begin
+// while the previous kernel on `s` finishes; see pdl_wait in qg_common.cuh),
+// plus a cluster of `cluster_x` CTAs along x when cluster_x > 0.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster_x > 0) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = (unsigned)cluster_x;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  lc.attrs = at;
+  lc.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&lc, kern, std::forward<Args>(args)...);
+  note_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // CUDA-core GEMV, 1..8 columns per launch: y = y0 + W x.
 cudaError_t cc_gemv(int qt, const void* q, const uint16_t* scl, int rows, int k,

@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_gate_up_kernel(const MoeDe
   constexpr int QB = QTraits<QT>::QB;
   const int n = p.ncols * p.topk;
   const int t = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();  // ids and x come from earlier kernels on the stream
 
   // Pair order: valid positions by (expert id, position), then the shared
   // expert's columns (codes n + c).
@@ -221,6 +223,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_down_kernel(const MoeDev p
   float* hs = reinterpret_cast<float*>(smem_f4);
   constexpr int QB = QTraits<QT>::QB;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  pdl_trigger();
+  pdl_wait();  // ids, rw, y0 and the gate/up results come from earlier kernels
   const int nparts = gridDim.x / p.ncols;
   const int c = blockIdx.x % p.ncols, part = blockIdx.x / p.ncols;
   if (part >= nparts) return;  // uniform over the CTA
@@ -343,9 +347,7 @@ static cudaError_t launch_moe(K kern, long grid_max_units, int multiple, size_t 
   if (grid > grid_max_units) grid = grid_max_units;
   grid = grid / multiple * multiple;
   if (grid < multiple) grid = multiple;
-  kern<<<(unsigned)grid, MOE_THREADS, smem, s>>>(d);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(MOE_THREADS), smem, s, 0, d);
 }
 
 template <int QT>

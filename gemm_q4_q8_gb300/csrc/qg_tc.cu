@@ -232,21 +232,15 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   __syncthreads();
 
   const bool producer = warp == TC_WARP_TMA;
+  // No early trigger here: a kernel that starts on an SM while this kernel's
+  // CTAs are resident inherits their shared-memory carve-out, and the
+  // CUDA-core kernels stream far slower with that little L1 left. Dependents
+  // launch when this grid completes.
   if (producer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
-      // stage s and phase bit ph advance incrementally (no division in the loop)
-      for (int i = 0, s = 0, ph = 0; i < nu; ++i, s = s + 1 == ns ? 0 : s + 1, ph ^= s == 0) {
-        if (i >= ns && !mbar_wait(&empty[s], (uint32_t)(ph ^ 1))) break;
+      auto load_weights = [&](int s, int u) {
         uint8_t* st = stages + (size_t)s * S::STAGE;
-        const int u = u0 + i;
-        mbar_expect_tx(&full[s], (uint32_t)(S::AS_BYTES + S::X_BYTES));
-        // x[0..CPAD)[u*256 .. u*256+256) as [4][CPAD][64] (3-D map, see tc_launch)
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(st + S::AS_BYTES)),
-            "l"(&mX), "r"(0), "r"(0), "r"(u * 4), "r"(smem_u32(&full[s]))
-            : "memory");
 #pragma unroll
         for (int m = 0; m < S::NMAT; ++m) {
           const CUtensorMap* mA = m == 0 ? &mA0 : &mA1;
@@ -257,6 +251,31 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
             tma_load_2d(a + bx * TC_BM * 128, mA, u * S::QROW + bx * 128, m0, &full[s], pol_w);
           tma_load_2d(st + S::NMAT * S::A_BYTES + m * S::S_BYTES, mS, u * 8, m0, &full[s], pol_w);
         }
+      };
+      auto load_x = [&](int s, int u) {
+        // x[0..CPAD)[u*256 .. u*256+256) as [4][CPAD][64] (3-D map, see tc_launch)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(stages + (size_t)s * S::STAGE + S::AS_BYTES)),
+            "l"(&mX), "r"(0), "r"(0), "r"(u * 4), "r"(smem_u32(&full[s]))
+            : "memory");
+      };
+      // The weights of the first ring's worth of stages are requested before
+      // waiting for the previous kernel on the stream (it never writes them);
+      // their x follows the wait.
+      const int npre = nu < ns ? nu : ns;
+      for (int i = 0; i < npre; ++i) {
+        mbar_expect_tx(&full[i], (uint32_t)(S::AS_BYTES + S::X_BYTES));
+        load_weights(i, u0 + i);
+      }
+      pdl_wait();
+      for (int i = 0; i < npre; ++i) load_x(i, u0 + i);
+      // stage s and phase bit ph advance incrementally (no division in the loop)
+      for (int i = npre, s = 0, ph = 1; i < nu; ++i, s = s + 1 == ns ? 0 : s + 1, ph ^= s == 0) {
+        if (!mbar_wait(&empty[s], (uint32_t)(ph ^ 1))) break;
+        mbar_expect_tx(&full[s], (uint32_t)(S::AS_BYTES + S::X_BYTES));
+        load_x(s, u0 + i);
+        load_weights(s, u0 + i);
       }
     }
     __syncwarp();
@@ -398,6 +417,9 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     }
   }
 
+  // y0, y and h are read or written only after every earlier kernel on the
+  // stream has finished
+  pdl_wait();
   // ---- reduce the two k-groups (fixed order: kj 0 + kj 1) in shared memory
   float* scratch = reinterpret_cast<float*>(stages);
   if (!producer) {
@@ -615,22 +637,9 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
   if (e != cudaSuccess) return e;
   const int ntile = (rows + TC_BM - 1) / TC_BM;
-  cudaLaunchConfig_t lc{};
-  lc.gridDim = dim3((unsigned)(ntile * cfg.ksplit), 1, 1);
-  lc.blockDim = dim3(TC_THREADS, 1, 1);
-  lc.dynamicSmemBytes = cfg.smem;
-  lc.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = (unsigned)cfg.ksplit;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, kern, mA0, mS0, mA1, mS1, mX, p);
-  note_launch();
   (void)S::NF;
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)(ntile * cfg.ksplit)), dim3(TC_THREADS), cfg.smem, s,
+                    cfg.ksplit, mA0, mS0, mA1, mS1, mX, p);
 }
 
 }  // namespace

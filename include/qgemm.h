@@ -37,6 +37,13 @@
  *    y0 == y is allowed (in-place y += W x). Any other overlap of y0 and y is
  *    QG_ERR_ALIAS.
  *  - rows == 0 is a valid empty problem: QG_OK, nothing launched.
+ *  - Kernels are launched with programmatic dependent launch: a call's kernels
+ *    may start while the previous kernel on `stream` is finishing, and until
+ *    that kernel has completed they read only the weight arrays (quants and
+ *    scales), never X, y0, ids or outputs. So weights must not be written by
+ *    a preceding kernel on the stream that itself lets its dependents start
+ *    early (one that calls cudaTriggerProgrammaticLaunchCompletion before its
+ *    last write). Ordinary kernels, and qrepack, never do.
  *  - Results are deterministic: the reduction order depends only on the
  *    problem shape, never on timing or on the number of SMs.
  *  - Arithmetic: weights are dequantised exactly (every Q4_0/Q8_0 weight is
