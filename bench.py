@@ -49,6 +49,26 @@ WORKLOAD = ("hot-path pass: Q4_0 GEMV 5120x5120 C=1 +y0; Q8_0 LM head 248320x512
 KERNELS = ("gemv", "lmhead", "twins", "gateup", "down", "moe")
 
 
+def lmhead_traffic(rows: int):
+    """DRAM bytes per LM-head launch from the committed ncu record
+    (profiles/lmhead_q8_gemv_traffic.json), scaled to `rows`; None when the
+    kernel's sources changed since the counters were taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "lmhead_q8_gemv_traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p))
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        fp = os.path.join(ROOT, f)
+        if not os.path.exists(fp):
+            return None
+        h.update(open(fp, "rb").read())
+    if h.hexdigest() != rec["sources_sha256"]:
+        return None
+    return rec["traffic_bytes_per_row"] * rows
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -86,7 +106,7 @@ def weight_bytes(w: dict, uniq_count: int) -> dict:
 class GpuStep:
     """Device-resident buffers and the six calls of one step."""
 
-    def __init__(self, w: dict, torch):
+    def __init__(self, w: dict, torch, only=None):
         import gemm_q4_q8_gb300 as qg
         self.qg = qg
         self.torch = torch
@@ -107,27 +127,32 @@ class GpuStep:
             del blocks
             return qd, sd
 
-        g = w["gemv"]
-        self.g_q, self.g_s = dq(synth.Q4_0, g["q"], g["scl"])
-        l = w["lmhead"]
-        self.l_q, self.l_s = dq(synth.Q8_0, l["q"], l["scl"])
-        tw = w["twins"]
-        self.t_q, self.t_s = dq(synth.Q4_0, tw["q"], tw["scl"])
-        f = w["ffn"]
-        self.f_qg, self.f_sg = dq(f["qtype"], f["qg"], f["sg"])
-        self.f_qu, self.f_su = dq(f["qtype"], f["qu"], f["su"])
-        self.f_qd, self.f_sd = dq(f["qtype"], f["qd"], f["sd"])
-        m = w["moe"]
-        self.m = {}
-        for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
-            self.m[a], self.m[b] = dq(m["qtype"], m[a], m[b])
-        self.m_sh = {}
-        for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
-            self.m_sh[a], self.m_sh[b] = dq(m["qtype"], m["shared"][a], m["shared"][b])
-        ws = qg.qmoe_workspace_bytes(m["n_expert"], m["ffn"], m["hidden"], m["ncols"], m["topk"])
-        self.m_ws = t.empty(ws, dtype=t.uint8, device="cuda")
-        self.m_err = t.zeros(1, dtype=t.int32, device="cuda")
-        self.m_uniq = t.empty(m["ncols"] * m["topk"], dtype=t.int32, device="cuda")
+        def want(*names):
+            return only is None or only in names
+
+        g, l, tw, f, m = w["gemv"], w["lmhead"], w["twins"], w["ffn"], w["moe"]
+        if want("gemv"):
+            self.g_q, self.g_s = dq(synth.Q4_0, g["q"], g["scl"])
+        if want("lmhead"):
+            self.l_q, self.l_s = dq(synth.Q8_0, l["q"], l["scl"])
+        if want("twins"):
+            self.t_q, self.t_s = dq(synth.Q4_0, tw["q"], tw["scl"])
+        if want("gateup"):
+            self.f_qg, self.f_sg = dq(f["qtype"], f["qg"], f["sg"])
+            self.f_qu, self.f_su = dq(f["qtype"], f["qu"], f["su"])
+        if want("down"):
+            self.f_qd, self.f_sd = dq(f["qtype"], f["qd"], f["sd"])
+        if want("moe"):
+            self.m = {}
+            for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
+                self.m[a], self.m[b] = dq(m["qtype"], m[a], m[b])
+            self.m_sh = {}
+            for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
+                self.m_sh[a], self.m_sh[b] = dq(m["qtype"], m["shared"][a], m["shared"][b])
+            ws = qg.qmoe_workspace_bytes(m["n_expert"], m["ffn"], m["hidden"], m["ncols"], m["topk"])
+            self.m_ws = t.empty(ws, dtype=t.uint8, device="cuda")
+            self.m_err = t.zeros(1, dtype=t.int32, device="cuda")
+            self.m_uniq = t.empty(m["ncols"] * m["topk"], dtype=t.int32, device="cuda")
 
         # per-step inputs (device) and their pinned host copies (for e2e)
         self.host_in = {
@@ -142,9 +167,9 @@ class GpuStep:
                        for k, v in self.host_in.items()}
         f16 = t.float16
         self.out = {
-            "g_y": t.empty((1, 5120), dtype=t.float32, device="cuda"),
-            "l_y": t.empty((1, l["rows"]), dtype=t.float32, device="cuda"),
-            "t_y": t.empty((8, 17408), dtype=t.float32, device="cuda"),
+            "g_y": t.empty((1, g["scl"].shape[0]), dtype=t.float32, device="cuda"),
+            "l_y": t.empty((1, l["scl"].shape[0]), dtype=t.float32, device="cuda"),
+            "t_y": t.empty((8, tw["scl"].shape[0]), dtype=t.float32, device="cuda"),
             "f_h": t.empty((16, 17408), dtype=f16, device="cuda"),
             "f_y": t.empty((16, 5120), dtype=t.float32, device="cuda"),
             "m_y": t.empty((8, 2048), dtype=t.float32, device="cuda"),
@@ -341,6 +366,32 @@ def max_over_ranks(v: float, world: int, torch, device) -> float:
     return float(t.item())
 
 
+def run_case(args):
+    """Profiling target: one call of the step, `--steps` times back to back, at
+    full size or with its matrix cut to `--case-rows` rows; prints nothing but
+    'ok'. For ncu captures of a single kernel on a case smaller than the step."""
+    import torch
+    import gemm_q4_q8_gb300 as qg
+    from gemm_q4_q8_gb300 import build
+    build.build()
+    w = make_workload(0)
+    if args.case_rows:
+        for key in ("gemv", "lmhead", "twins"):
+            c = w[key]
+            r = min(args.case_rows, c["scl"].shape[0])
+            c["q"], c["scl"] = c["q"][:r], c["scl"][:r]
+            if c.get("y0") is not None:
+                c["y0"] = c["y0"][:, :r]
+            c["rows"] = r
+    gs = GpuStep(w, torch, only=args.case)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.steps):
+        gs.call(args.case, stream)
+    torch.cuda.synchronize()
+    print("ok", args.case)
+    return 0
+
+
 def run_reference(args):
     """The oracle timed on this host's cores (the reference arm of this tier)."""
     rank, world, _ = dist_env()
@@ -383,11 +434,16 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--ref-frac", type=float, default=1 / 256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=KERNELS, default=None,
+                    help="profiling target: run only this call (see run_case)")
+    ap.add_argument("--case-rows", type=int, default=0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.case:
+        return run_case(args)
 
     import torch
     rank, world, local = dist_env()
@@ -520,7 +576,9 @@ def main(argv=None):
         "roofline": {"kernel": "lmhead (qgemv_q8_0, 248320x5120, 1 column)", "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": None},
+                     "traffic": lmhead_traffic(w["lmhead"]["rows"]),
+                     "traffic_note": "dram read+write bytes per launch, ncu capture of a "
+                                     "65,536-row cut scaled by rows (profiles/lmhead_q8_gemv.md)"},
         "breakdown": breakdown,
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
