@@ -78,6 +78,15 @@ def test_lm_head_sampled_rows():
     check_case(case, rows_sel=sel, what="Q8_0 LM head 248320x5120 (sampled rows)")
 
 
+def test_q4_large_one_column_sampled_rows():
+    """One column of a large Q4_0 matrix (the tensor-core plan), ragged row tail."""
+    case = synth.gemv_case(synth.Q4_0, 20000, 5120, 1, residual=True, seed=41)
+    g = np.random.Generator(np.random.PCG64(7))
+    sel = np.unique(np.concatenate([np.arange(64), 20000 - 96 + np.arange(96),
+                                    g.integers(0, 20000, 2048)]))
+    check_case(case, rows_sel=sel, what="Q4_0 20000x5120 C=1 (sampled rows)")
+
+
 @pytest.mark.parametrize("rows", [5120, 17408])
 @pytest.mark.parametrize("ncols", [2, 4, 8])
 def test_twins(rows, ncols):
