@@ -392,6 +392,175 @@ def run_case(args):
     return 0
 
 
+# ------------------------------------------------------------ per-config
+CONFIGS = (
+    # name, kind, qtype, rows, k, ncols, residual
+    ("q8_gemv_2048_c1", "gemv", synth.Q8_0, 2048, 2048, 1, False),
+    ("q4_gemv_5120_c1_y0", "gemv", synth.Q4_0, 5120, 5120, 1, True),
+    ("q8_lmhead_248320_c1", "gemv", synth.Q8_0, 248320, 5120, 1, False),
+    ("q4_twins_5120_c2", "gemv", synth.Q4_0, 5120, 5120, 2, False),
+    ("q4_twins_5120_c4", "gemv", synth.Q4_0, 5120, 5120, 4, False),
+    ("q4_twins_5120_c8", "gemv", synth.Q4_0, 5120, 5120, 8, False),
+    ("q4_twins_17408_c2", "gemv", synth.Q4_0, 17408, 5120, 2, False),
+    ("q4_twins_17408_c4", "gemv", synth.Q4_0, 17408, 5120, 4, False),
+    ("q4_twins_17408_c8", "gemv", synth.Q4_0, 17408, 5120, 8, False),
+    ("q4_ffn_gateup_17408_c16", "gateup", synth.Q4_0, 17408, 5120, 16, False),
+    ("q4_ffn_down_5120x17408_c16_y0", "cols", synth.Q4_0, 5120, 17408, 16, True),
+    ("q8_moe_c1", "moe", synth.Q8_0, 0, 0, 1, False),
+    ("q8_moe_c8", "moe", synth.Q8_0, 0, 0, 8, False),
+)
+L2_BYTES = 129 * 2**20
+
+
+def run_configs(args):
+    """Each config of the workload alone: CUDA-graph replays of back-to-back
+    calls that cycle through enough distinct weight copies (>= 4x L2, or one
+    copy when a single one is larger) that L2 holds none of them; MoE calls
+    cycle through 8 id sets. 20 warm-up calls; per replay, the mean call time;
+    median and p10/p90 over the replays. Beside it, the oracle's time per
+    call (rows sampled and scaled; 1 thread and all host threads). One JSON
+    line per config."""
+    import torch
+    import gemm_q4_q8_gb300 as qg
+    import oracle
+    from gemm_q4_q8_gb300 import build
+    build.build()
+    oracle.build()
+    peak, peak_kind = peaks()
+    stream = torch.cuda.current_stream()
+    ncores = os.cpu_count() or 1
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def dq(qtype, q, scl):
+        rows, nb = scl.shape
+        blocks = d(synth.to_gguf_blocks(qtype, q, scl))
+        qd = torch.empty(q.shape, dtype=torch.uint8, device="cuda")
+        sd = torch.empty(scl.shape, dtype=torch.int16, device="cuda")
+        qg.qrepack(qtype, blocks, rows, nb * 32, qd, sd)
+        torch.cuda.synchronize()
+        return qd, sd
+
+    def oracle_us(fn, frac):
+        t0 = time.perf_counter()
+        fn()
+        return (time.perf_counter() - t0) / frac * 1e6
+
+    for name, kind, qt, rows, k, ncols, residual in CONFIGS:
+        if args.config_filter and args.config_filter not in name:
+            continue
+        g = synth.rng(1)
+        calls = []
+        if kind == "moe":
+            m = synth.moe_layer(ncols, seed=2)
+            dm = {}
+            for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
+                dm[a], dm[b] = dq(qt, m[a], m[b])
+            sh = {}
+            for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
+                sh[a], sh[b] = dq(qt, m["shared"][a], m["shared"][b])
+            ws = torch.empty(qg.qmoe_workspace_bytes(256, 512, 2048, ncols, 8), dtype=torch.uint8,
+                             device="cuda")
+            gi = synth.rng(9)
+            idn = [np.stack([gi.choice(256, 8, replace=False) for _ in range(ncols)]).astype(np.int32)
+                   for _ in range(8)]
+            uniq = float(np.mean([len(np.unique(i)) for i in idn]))
+            wbytes = (uniq + 1) * 3 * synth.weight_bytes(qt, 512, 2048)
+            ids = [d(i) for i in idn]
+            rw, x = d(m["rw"]), d(m["x"].view(np.int16)).view(torch.float16)
+            y = torch.empty((ncols, 2048), dtype=torch.float32, device="cuda")
+            for i in range(8):
+                calls.append(lambda s, i=i: qg.qmoe_experts(
+                    qt, dm["qg"], dm["sg"], dm["qu"], dm["su"], dm["qd"], dm["sd"], 256, 512, 2048,
+                    ids[i], rw, x, y, ws, shared=sh, stream=s))
+            o_frac = 1.0
+            o_fn = {t: (lambda t=t: oracle.moe(m, nthreads=t)) for t in (1, ncores)}
+            extra = {"distinct_experts_mean": uniq}
+        else:
+            nmat = 2 if kind == "gateup" else 1
+            wb1 = nmat * synth.weight_bytes(qt, rows, k)
+            ncopy = int(min(16, max(1, np.ceil(4 * L2_BYTES / wb1))))
+            mats = [synth.draw_matrix(g, qt, rows, k) for _ in range(nmat)]
+            x_np = synth.draw_x(g, ncols, k)
+            y0_np = synth.draw_y0(g, ncols, rows) if residual else None
+            dev_mats = [[dq(qt, q, sc) for (q, sc) in mats] for _ in range(ncopy)]
+            x = d(x_np.view(np.int16)).view(torch.float16)
+            y0 = d(y0_np) if residual else None
+            if kind == "gateup":
+                h = torch.empty((ncols, rows), dtype=torch.float16, device="cuda")
+                for c in range(ncopy):
+                    (a, sa), (b, sb) = dev_mats[c]
+                    calls.append(lambda s, a=a, sa=sa, b=b, sb=sb: qg.qffn_gate_up_silu(
+                        qt, a, sa, b, sb, x, h, s))
+            else:
+                y = torch.empty((ncols, rows), dtype=torch.float32, device="cuda")
+                fn = qg.qgemm_cols if kind == "cols" else (
+                    qg.qgemv_q4_0 if qt == synth.Q4_0 else qg.qgemv_q8_0)
+                for c in range(ncopy):
+                    (a, sa), = dev_mats[c]
+                    if kind == "cols":
+                        calls.append(lambda s, a=a, sa=sa: fn(qt, a, sa, x, y, y0, s))
+                    else:
+                        calls.append(lambda s, a=a, sa=sa: fn(a, sa, x, y, y0, s))
+            wbytes = wb1
+            # the oracle runs on an evenly spaced row sample of about 25 M weights
+            # (the whole matrix when it is smaller), its time scaled to all rows
+            n_s = max(1, min(rows, int(25e6 / (nmat * k))))
+            sel = np.linspace(0, rows - 1, n_s).astype(np.int64)
+            o_frac = n_s / rows
+            if kind == "gateup":
+                (q1, s1), (q2, s2) = mats
+                o_fn = {t: (lambda t=t: oracle.ffn_gate_up_silu(qt, q1[sel], s1[sel], q2[sel], s2[sel],
+                                                                x_np, nthreads=t)) for t in (1, ncores)}
+            else:
+                (q1, s1), = mats
+                o_fn = {t: (lambda t=t: oracle.matmul(qt, q1, s1, x_np, y0_np, rows_sel=sel,
+                                                      nthreads=t)) for t in (1, ncores)}
+            extra = {"weight_copies": ncopy}
+        # graph of back-to-back calls cycling the copies
+        reps = max(len(calls), 16)
+        gcap = torch.cuda.Stream()
+        with torch.cuda.stream(gcap):
+            for i in range(20):
+                calls[i % len(calls)](gcap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gcap):
+            for i in range(reps):
+                calls[i % len(calls)](gcap)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        nrep = max(13, -(-200 // reps))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nrep)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        per_call = np.array([e0.elapsed_time(e1) * 1e3 / reps for e0, e1 in evs])
+        med = float(np.median(per_call))
+        o1 = oracle_us(o_fn[1], o_frac)
+        on = oracle_us(o_fn[ncores], o_frac)
+        line = {
+            "config": name, "us_median": med,
+            "us_p10": float(np.percentile(per_call, 10)), "us_p90": float(np.percentile(per_call, 90)),
+            "timed_calls": int(nrep * reps), "weight_bytes": wbytes,
+            "GBps": wbytes / (med * 1e-6) / 1e9,
+            "frac_of_measured_hbm": wbytes / (med * 1e-6) / 1e9 / peak, "peak_kind": peak_kind,
+            "frac_of_8TBps_nominal": wbytes / (med * 1e-6) / 8e12,
+            "oracle_us_1thread": o1, "oracle_us_all_threads": on, "oracle_threads": ncores,
+            "oracle_sample": ("whole layer" if kind == "moe" else f"{o_frac:.3f} of the rows, scaled"),
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+        del calls, graph
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_reference(args):
     """The oracle timed on this host's cores (the reference arm of this tier)."""
     rank, world, _ = dist_env()
@@ -437,6 +606,9 @@ def main(argv=None):
     ap.add_argument("--case", choices=KERNELS, default=None,
                     help="profiling target: run only this call (see run_case)")
     ap.add_argument("--case-rows", type=int, default=0)
+    ap.add_argument("--configs", action="store_true",
+                    help="time every workload config alone (one JSON line each)")
+    ap.add_argument("--config-filter", default="")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -444,6 +616,8 @@ def main(argv=None):
         return run_reference(args)
     if args.case:
         return run_case(args)
+    if args.configs:
+        return run_configs(args)
 
     import torch
     rank, world, local = dist_env()
