@@ -59,8 +59,11 @@ def lib():
                                C.POINTER(_Expert), vp, i32, vp, vp, dp, dp, vp,
                                C.POINTER(C.c_int), i32]
         L.qref_repack.argtypes = [i32, vp, i32, i32, vp, vp]
+        L.qref_argmax.argtypes = [vp, i32, i32, vp, vp]
+        L.qref_topk.argtypes = [vp, i32, i32, i32, vp, vp]
         for f in ("qref_dequant_row", "qref_matmul", "qref_matmul_rows",
-                  "qref_ffn_gate_up_silu", "qref_moe", "qref_repack"):
+                  "qref_ffn_gate_up_silu", "qref_moe", "qref_repack", "qref_argmax",
+                  "qref_topk"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -187,3 +190,29 @@ def repack(qtype: int, gguf: np.ndarray, rows: int, k: int):
     if qtype == Q8_0:
         q = q.view(np.int8)
     return q, s
+
+
+def argmax(x: np.ndarray):
+    """Greedy argmax of each row of f32 x [ncols, n]: (idx int32 [ncols], val f32 [ncols]).
+    Order: numbers before NaN, larger first, ties (and NaNs) by lower index."""
+    x = _c(np.atleast_2d(x), np.float32)
+    ncols, n = x.shape
+    idx = np.empty(ncols, dtype=np.int32)
+    val = np.empty(ncols, dtype=np.float32)
+    rc = lib().qref_argmax(_p(x), n, ncols, _p(idx), _p(val))
+    if rc:
+        raise ValueError(f"qref_argmax rc={rc}")
+    return idx, val
+
+
+def topk(x: np.ndarray, k: int):
+    """Top-k of each row of f32 x [ncols, n] in rank order (the argmax order):
+    (idx int32 [ncols, k], val f32 [ncols, k])."""
+    x = _c(np.atleast_2d(x), np.float32)
+    ncols, n = x.shape
+    idx = np.empty((ncols, k), dtype=np.int32)
+    val = np.empty((ncols, k), dtype=np.float32)
+    rc = lib().qref_topk(_p(x), n, ncols, k, _p(idx), _p(val))
+    if rc:
+        raise ValueError(f"qref_topk rc={rc}")
+    return idx, val

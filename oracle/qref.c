@@ -31,6 +31,9 @@
  *    section "A mixture of experts is a different animal").
  *  - Repack: GGUF interleaved blocks into separate quant and scale arrays
  *    ("Architecture", section "Memory and caching").
+ *  - Sampling: greedy argmax and top-k over f32 logits, lowest index on ties
+ *    ("Engine and kernels", sections "Kernel families", sampling, and "Fewer
+ *    passes", GPU argmax and top-k).
  *
  * Pins (tests/test_oracle_pins.py): hand-worked blocks, x = e_j returning
  * dequantised column j, nibble 8 / scale 0 giving zero, linearity in x,
@@ -366,5 +369,56 @@ int qref_repack(int type, const uint8_t *gguf, int rows, int k, uint8_t *q_out,
           for (int h = 0; h < 2; ++h) dst[g + 2 * m + h] = blk[2 + g + m + 8 * h];
     }
   }
+  return 0;
+}
+
+/* ----------------------------------------------------------- sampling */
+
+/* Order of the sampling calls ("Engine and kernels", section "Fewer passes":
+ * lowest-index tie-breaking, as a CPU loop would do it): a number ranks before
+ * NaN; among numbers the larger value ranks first (+0 and -0 are equal); equal
+ * values, and two NaNs, rank by the lower index. Returns 1 when element i
+ * ranks before element j. */
+static int qref_before(const float *v, int64_t i, int64_t j) {
+  const float a = v[i], b = v[j];
+  const int na = isnan(a) != 0, nb = isnan(b) != 0;
+  if (na != nb) return nb;
+  if (!na && a != b) return a > b;
+  return i < j;
+}
+
+/* Greedy argmax of every column of x [ncols][n]: the first-ranked element. */
+int qref_argmax(const float *x, int n, int ncols, int32_t *idx, float *val) {
+  if (n < 1 || ncols < 1) return 1;
+  for (int c = 0; c < ncols; ++c) {
+    const float *v = x + (size_t)c * n;
+    int64_t best = 0;
+    for (int64_t i = 1; i < n; ++i)
+      if (qref_before(v, i, best)) best = i;
+    idx[c] = (int32_t)best;
+    if (val) val[c] = v[best];
+  }
+  return 0;
+}
+
+/* Top-k of every column: k selection passes, each taking the first-ranked
+ * element not yet taken; outputs [ncols][k] in rank order. */
+int qref_topk(const float *x, int n, int ncols, int k, int32_t *idx, float *val) {
+  if (n < 1 || ncols < 1 || k < 1 || k > n) return 1;
+  unsigned char *taken = (unsigned char *)malloc((size_t)n);
+  if (!taken) return 2;
+  for (int c = 0; c < ncols; ++c) {
+    const float *v = x + (size_t)c * n;
+    memset(taken, 0, (size_t)n);
+    for (int r = 0; r < k; ++r) {
+      int64_t best = -1;
+      for (int64_t i = 0; i < n; ++i)
+        if (!taken[i] && (best < 0 || qref_before(v, i, best))) best = i;
+      taken[best] = 1;
+      idx[(size_t)c * k + r] = (int32_t)best;
+      if (val) val[(size_t)c * k + r] = v[best];
+    }
+  }
+  free(taken);
   return 0;
 }

@@ -342,3 +342,37 @@ def test_h_bound_dominates_f16_rounding(oracle_lib):
     h = g * (1.0 + np.tanh(g / 2.0)) / 2.0 * u
     h16 = h.astype(np.float16).astype(np.float64)
     assert np.all(np.abs(h16 - h) <= b)
+
+
+def _golden_vec(vals):
+    return np.array([float(v) for v in vals], dtype=np.float32)
+
+
+def test_golden_sampling(oracle_lib):
+    for case in json.load(open(GOLDEN))["sampling"]["cases"]:
+        x = _golden_vec(case["x"])
+        idx, val = oracle_lib.argmax(x[None, :])
+        assert int(idx[0]) == case["argmax"], case
+        tidx, tval = oracle_lib.topk(x[None, :], x.size)
+        assert tidx[0].tolist() == case["topk_idx"], case
+        assert np.array_equal(tval[0], x[tidx[0]], equal_nan=True)
+
+
+def test_sampling_matches_numpy_orderings(oracle_lib):
+    """Against numpy's first-occurrence argmax and a lexicographic sort on
+    (NaN last, value descending, index ascending), with many ties."""
+    g = np.random.Generator(np.random.PCG64(5))
+    for n in (1, 7, 300, 4096):
+        x = g.integers(-6, 6, size=(3, n)).astype(np.float32) * 0.5
+        x[1, ::7] = np.nan
+        x[2, :] = np.where(g.random(n) < 0.3, -0.0, x[2, :]).astype(np.float32)
+        idx, val = oracle_lib.argmax(x)
+        k = min(n, 37)
+        tidx, tval = oracle_lib.topk(x, k)
+        for c in range(3):
+            v = x[c]
+            order = np.lexsort((np.arange(n), -np.nan_to_num(v, nan=0.0), np.isnan(v)))
+            assert tidx[c].tolist() == order[:k].tolist()
+            assert int(idx[c]) == int(order[0])
+            if not np.isnan(v).all():
+                assert int(idx[c]) == int(np.nanargmax(v))
