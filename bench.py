@@ -408,6 +408,11 @@ CONFIGS = (
     ("q4_ffn_down_5120x17408_c16_y0", "cols", synth.Q4_0, 5120, 17408, 16, True),
     ("q8_moe_c1", "moe", synth.Q8_0, 0, 0, 1, False),
     ("q8_moe_c8", "moe", synth.Q8_0, 0, 0, 8, False),
+    # sampling over LM-head logits (next steps after the LM head): rows = n, k = top-k
+    ("argmax_lmhead_248320_c1", "argmax", None, 248320, 1, 1, False),
+    ("argmax_lmhead_248320_c8", "argmax", None, 248320, 1, 8, False),
+    ("topk40_lmhead_248320_c1", "topk", None, 248320, 40, 1, False),
+    ("topk40_lmhead_248320_c8", "topk", None, 248320, 40, 8, False),
 )
 L2_BYTES = 129 * 2**20
 
@@ -452,7 +457,23 @@ def run_configs(args):
             continue
         g = synth.rng(1)
         calls = []
-        if kind == "moe":
+        if kind in ("argmax", "topk"):
+            n, kk = rows, k
+            xs_np = [g.standard_normal((ncols, n)).astype(np.float32) for _ in range(4)]
+            xs_d = [d(a) for a in xs_np]
+            ib = torch.empty((ncols, kk), dtype=torch.int32, device="cuda")
+            vb = torch.empty((ncols, kk), dtype=torch.float32, device="cuda")
+            for a in xs_d:
+                if kind == "argmax":
+                    calls.append(lambda s, a=a: qg.qargmax_f32(a, ib[:, 0], vb[:, 0], s))
+                else:
+                    calls.append(lambda s, a=a: qg.qtopk_f32(a, kk, ib, vb, s))
+            wbytes = ncols * n * 4  # logits read (no weights)
+            o_frac = 1.0
+            o_fn = {t: ((lambda: oracle.argmax(xs_np[0])) if kind == "argmax"
+                        else (lambda: oracle.topk(xs_np[0], kk))) for t in (1, ncores)}
+            extra = {"bytes_are": "logits read", "k": kk}
+        elif kind == "moe":
             m = synth.moe_layer(ncols, seed=2)
             dm = {}
             for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemm.so")
 
 EXPORTS = ("qg_status_str", "qgemv_q4_0", "qgemv_q8_0", "qgemm_cols", "qffn_gate_up_silu",
            "qmoe_workspace_bytes", "qmoe_experts", "qmoe_experts_noalloc", "qrepack",
-           "qg_kernel_launches")
+           "qargmax_f32", "qtopk_f32", "qg_kernel_launches")
 
 QG_MOE_NOALLOC_WS_BYTES = 8 << 20
 
@@ -66,6 +66,8 @@ def load(path: str | None = None):
     L.qmoe_experts_noalloc.argtypes = [i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32,
                                        C.POINTER(QGExpert), vp, i32, vp, vp, vp, vp, vp]
     L.qrepack.argtypes = [i32, vp, i32, i32, vp, vp, vp]
+    L.qargmax_f32.argtypes = [vp, i32, i32, vp, vp, vp]
+    L.qtopk_f32.argtypes = [vp, i32, i32, i32, vp, vp, vp]
     L.qg_kernel_launches.argtypes = []
     L.qg_kernel_launches.restype = C.c_uint64
     for f in EXPORTS:
@@ -165,3 +167,19 @@ def qrepack(qtype, gguf, rows, k, q_out, scl_out, stream=None):
     """GGUF interleaved blocks (device bytes) -> quant and scale arrays."""
     _check("qrepack", load().qrepack(int(qtype), _ptr(gguf), rows, k, _ptr(q_out), _ptr(scl_out),
                                      _stream(stream)))
+
+
+def qargmax_f32(x, idx_out, val_out=None, stream=None):
+    """Greedy argmax of each row of f32 x [ncols, n] (numbers before NaN, larger
+    first, ties by lower index): idx_out int32 [ncols], val_out f32 [ncols] or None."""
+    ncols, n = x.shape
+    _check("qargmax_f32", load().qargmax_f32(_ptr(x), n, ncols, _ptr(idx_out), _ptr(val_out),
+                                             _stream(stream)))
+
+
+def qtopk_f32(x, k, idx_out, val_out=None, stream=None):
+    """The k first-ranked elements of each row of f32 x [ncols, n], in rank order
+    (the argmax order): idx_out int32 [ncols, k], val_out f32 [ncols, k] or None."""
+    ncols, n = x.shape
+    _check("qtopk_f32", load().qtopk_f32(_ptr(x), n, ncols, int(k), _ptr(idx_out), _ptr(val_out),
+                                         _stream(stream)))

@@ -193,6 +193,26 @@ qg_status qmoe_experts(qg_type t, const void* qg, const uint16_t* sg, const void
   return from_cuda(qg::moe_forward(a, stream));
 }
 
+qg_status qargmax_f32(const float* x, int n, int ncols, int32_t* idx_out, float* val_out,
+                      cudaStream_t stream) {
+  if (n < 1 || ncols < 1 || ncols > 64) return QG_ERR_SHAPE;
+  if (!x || !idx_out) return QG_ERR_NULL;
+  if (!aligned(x, 4) || !aligned(idx_out, 4) || (val_out && !aligned(val_out, 4))) return QG_ERR_ALIGN;
+  qg_status st = check_device();
+  if (st != QG_OK) return st;
+  return from_cuda(qg::argmax_launch(x, n, ncols, idx_out, val_out, stream));
+}
+
+qg_status qtopk_f32(const float* x, int n, int ncols, int k, int32_t* idx_out, float* val_out,
+                    cudaStream_t stream) {
+  if (n < 1 || ncols < 1 || ncols > 64 || k < 1 || k > 256 || k > n) return QG_ERR_SHAPE;
+  if (!x || !idx_out) return QG_ERR_NULL;
+  if (!aligned(x, 4) || !aligned(idx_out, 4) || (val_out && !aligned(val_out, 4))) return QG_ERR_ALIGN;
+  qg_status st = check_device();
+  if (st != QG_OK) return st;
+  return from_cuda(qg::topk_launch(x, n, ncols, k, idx_out, val_out, stream));
+}
+
 qg_status qrepack(qg_type t, const void* gguf, int rows, int k, void* q_out,
                   uint16_t* scl_out, cudaStream_t stream) {
   if (!valid_type((int)t)) return QG_ERR_TYPE;

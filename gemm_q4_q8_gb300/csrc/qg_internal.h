@@ -91,4 +91,10 @@ cudaError_t moe_forward(const MoeArgs& a, cudaStream_t s);
 cudaError_t repack_launch(int qt, const void* gguf, int rows, int k, void* q_out,
                           uint16_t* scl_out, cudaStream_t s);
 
+// Greedy argmax / top-k over f32 columns [ncols][n] (qg_sample.cu).
+cudaError_t argmax_launch(const float* x, int n, int ncols, int32_t* idx, float* val,
+                          cudaStream_t s);
+cudaError_t topk_launch(const float* x, int n, int ncols, int k, int32_t* idx, float* val,
+                        cudaStream_t s);
+
 }  // namespace qg

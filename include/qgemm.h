@@ -202,6 +202,27 @@ qg_status qrepack(qg_type t, const void *gguf, int rows, int k, void *q_out,
                   uint16_t *scl_out, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Sampling over f32 logits ("Engine and kernels", section "Kernel families":
+ * greedy argmax and top-k on the GPU, so a token reads back a few bytes instead
+ * of the logits; section "Fewer passes": lowest-index tie-breaking).
+ *   x        : f32 [ncols][n], 4-byte aligned (e.g. the LM-head output of
+ *              qgemv_q8_0; its first n rows are the draft head's output)
+ *   n        : >= 1 values per column;  ncols: 1..64
+ *   Order    : a number ranks before NaN; larger values first; +0 equals -0;
+ *              equal values, and NaNs, rank by the lower index.
+ * qargmax_f32: idx_out int32 [ncols], the first-ranked element of each column;
+ *              val_out NULL or f32 [ncols], its value (the bits of x).
+ * qtopk_f32  : the k first-ranked elements of each column in rank order,
+ *              1 <= k <= 256, k <= n; idx_out int32 [ncols][k], val_out NULL
+ *              or f32 [ncols][k].
+ * Both are deterministic. QG_ERR_SHAPE for n, ncols or k out of range.
+ * ------------------------------------------------------------------------- */
+qg_status qargmax_f32(const float *x, int n, int ncols, int32_t *idx_out, float *val_out,
+                      cudaStream_t stream);
+qg_status qtopk_f32(const float *x, int n, int ncols, int k, int32_t *idx_out,
+                    float *val_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Diagnostics: number of kernels this library has launched in this process
  * (monotonic, all devices and threads). Lets a caller count the GPU launches of
  * a region of work. Not part of the method.

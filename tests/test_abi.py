@@ -127,3 +127,14 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
         pytest.skip("a GPU is present")
     # valid arguments: the library must fail loudly (no CPU fallback)
     assert gemv(lib) == 6
+
+
+def test_sampling_argument_errors(lib):
+    assert lib.qargmax_f32(ALIGNED, 0, 1, ALIGNED, None, None) == 2
+    assert lib.qargmax_f32(ALIGNED, 10, 65, ALIGNED, None, None) == 2
+    assert lib.qargmax_f32(None, 10, 1, ALIGNED, None, None) == 1
+    assert lib.qargmax_f32(ALIGNED + 2, 10, 1, ALIGNED, None, None) == 3
+    assert lib.qtopk_f32(ALIGNED, 10, 1, 11, ALIGNED, None, None) == 2
+    assert lib.qtopk_f32(ALIGNED, 1000, 1, 257, ALIGNED, None, None) == 2
+    assert lib.qtopk_f32(ALIGNED, 1000, 1, 0, ALIGNED, None, None) == 2
+    assert lib.qtopk_f32(ALIGNED, 1000, 1, 5, None, None, None) == 1
