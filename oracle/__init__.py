@@ -61,9 +61,11 @@ def lib():
         L.qref_repack.argtypes = [i32, vp, i32, i32, vp, vp]
         L.qref_argmax.argtypes = [vp, i32, i32, vp, vp]
         L.qref_topk.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.qref_router_logits.argtypes = [vp, vp, i32, i32, i32, dp, dp]
+        L.qref_softmax.argtypes = [vp, i32, dp]
         for f in ("qref_dequant_row", "qref_matmul", "qref_matmul_rows",
                   "qref_ffn_gate_up_silu", "qref_moe", "qref_repack", "qref_argmax",
-                  "qref_topk"):
+                  "qref_topk", "qref_router_logits", "qref_softmax"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -216,3 +218,28 @@ def topk(x: np.ndarray, k: int):
     if rc:
         raise ValueError(f"qref_topk rc={rc}")
     return idx, val
+
+
+def router_logits(w: np.ndarray, x: np.ndarray):
+    """(logits, S) in f64 [ncols, E]: logits = W_router x per column (w f32 [E, hidden],
+    x f16 bits [ncols, hidden]); S = sum |w||x| (for the product tolerance)."""
+    w = _c(w, np.float32)
+    x = _c(np.atleast_2d(x), np.uint16)
+    E, hidden = w.shape
+    ncols = x.shape[0]
+    lg = np.empty((ncols, E), dtype=np.float64)
+    S = np.empty_like(lg)
+    rc = lib().qref_router_logits(_p(w), _p(x), E, hidden, ncols, _p(lg), _p(S))
+    if rc:
+        raise ValueError(f"qref_router_logits rc={rc}")
+    return lg, S
+
+
+def softmax(v: np.ndarray) -> np.ndarray:
+    """f64 softmax of the f32 values v (1-D)."""
+    v = _c(np.ravel(v), np.float32)
+    out = np.empty(v.size, dtype=np.float64)
+    rc = lib().qref_softmax(_p(v), v.size, _p(out))
+    if rc:
+        raise ValueError(f"qref_softmax rc={rc}")
+    return out

@@ -34,6 +34,11 @@
  *  - Sampling: greedy argmax and top-k over f32 logits, lowest index on ties
  *    ("Engine and kernels", sections "Kernel families", sampling, and "Fewer
  *    passes", GPU argmax and top-k).
+ *  - MoE router: logits = W_router x per column (f32 router weights, the
+ *    f16/bf16 -> f32 conversion of "Architecture", section "Memory and
+ *    caching"), top-k experts in the sampling order, routing weights = a
+ *    softmax over the selected logits ("Engine and kernels", section "Kernel
+ *    families", MoE: router and top-k on the GPU).
  *
  * Pins (tests/test_oracle_pins.py): hand-worked blocks, x = e_j returning
  * dequantised column j, nibble 8 / scale 0 giving zero, linearity in x,
@@ -420,5 +425,41 @@ int qref_topk(const float *x, int n, int ncols, int k, int32_t *idx, float *val)
     }
   }
   free(taken);
+  return 0;
+}
+
+/* ---------------------------------------------------------- MoE router */
+
+/* Router logits in f64: logits[c][e] = sum_k w[e][k] * x[c][k] (w f32
+ * [E][hidden], x f16 bits [ncols][hidden]), k order; S[c][e] = sum |w||x|. */
+int qref_router_logits(const float *w, const uint16_t *x, int E, int hidden, int ncols,
+                       double *logits, double *S) {
+  if (E < 1 || hidden < 1 || ncols < 1) return 1;
+  for (int c = 0; c < ncols; ++c)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0, sa = 0.0;
+      for (int k = 0; k < hidden; ++k) {
+        const double p = (double)w[(size_t)e * hidden + k] * qref_f16_to_f64(x[(size_t)c * hidden + k]);
+        acc += p;
+        sa += fabs(p);
+      }
+      logits[(size_t)c * E + e] = acc;
+      if (S) S[(size_t)c * E + e] = sa;
+    }
+  return 0;
+}
+
+/* Softmax of k values in f64: out[i] = exp(v[i] - max) / sum_j exp(v[j] - max). */
+int qref_softmax(const float *v, int k, double *out) {
+  if (k < 1) return 1;
+  double m = v[0];
+  for (int i = 1; i < k; ++i)
+    if (v[i] > m) m = v[i];
+  double sum = 0.0;
+  for (int i = 0; i < k; ++i) {
+    out[i] = exp((double)v[i] - m);
+    sum += out[i];
+  }
+  for (int i = 0; i < k; ++i) out[i] /= sum;
   return 0;
 }

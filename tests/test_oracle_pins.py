@@ -376,3 +376,27 @@ def test_sampling_matches_numpy_orderings(oracle_lib):
             assert int(idx[c]) == int(order[0])
             if not np.isnan(v).all():
                 assert int(idx[c]) == int(np.nanargmax(v))
+
+
+def test_router_logits_against_numpy(oracle_lib):
+    g = np.random.Generator(np.random.PCG64(11))
+    w = g.standard_normal((37, 96)).astype(np.float32)
+    x = g.standard_normal((3, 96)).astype(np.float16)
+    lg, S = oracle_lib.router_logits(w, x.view(np.uint16))
+    ref = x.astype(np.float64) @ w.astype(np.float64).T
+    assert np.allclose(lg, ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(S, np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64)).T, rtol=1e-12)
+    # one-hot x picks a column of W exactly
+    e = np.zeros((1, 96), dtype=np.float16)
+    e[0, 5] = 1.0
+    lg1, _ = oracle_lib.router_logits(w, e.view(np.uint16))
+    assert np.array_equal(lg1[0], w[:, 5].astype(np.float64))
+
+
+def test_softmax_closed_forms(oracle_lib):
+    assert np.allclose(oracle_lib.softmax(np.zeros(8, np.float32)), np.full(8, 0.125), rtol=0, atol=1e-15)
+    p = oracle_lib.softmax(np.array([np.log(3.0), 0.0], np.float32))
+    l3 = float(np.float32(np.log(3.0)))
+    assert abs(p[0] - np.exp(l3) / (np.exp(l3) + 1.0)) < 1e-15 and abs(p.sum() - 1.0) < 1e-15
+    big = oracle_lib.softmax(np.array([1000.0, 999.0, -1000.0], np.float32))
+    assert abs(big[0] - 1.0 / (1.0 + np.exp(-1.0))) < 1e-12 and big[2] == 0.0
