@@ -413,6 +413,10 @@ CONFIGS = (
     ("argmax_lmhead_248320_c8", "argmax", None, 248320, 1, 8, False),
     ("topk40_lmhead_248320_c1", "topk", None, 248320, 40, 1, False),
     ("topk40_lmhead_248320_c8", "topk", None, 248320, 40, 8, False),
+    # MoE router (f32 [256, 2048] router weights) + top-8 + softmax: rows = experts
+    ("router_256x2048_top8_c1", "router", None, 256, 2048, 1, False),
+    ("router_256x2048_top8_c8", "router", None, 256, 2048, 8, False),
+    ("router_256x2048_top8_c16", "router", None, 256, 2048, 16, False),
 )
 L2_BYTES = 129 * 2**20
 
@@ -473,6 +477,25 @@ def run_configs(args):
             o_fn = {t: ((lambda: oracle.argmax(xs_np[0])) if kind == "argmax"
                         else (lambda: oracle.topk(xs_np[0], kk))) for t in (1, ncores)}
             extra = {"bytes_are": "logits read", "k": kk}
+        elif kind == "router":
+            E, hid = rows, k
+            wr_np = [(g.standard_normal((E, hid)) * 0.02).astype(np.float32) for _ in range(4)]
+            x_np = synth.draw_x(g, ncols, hid)
+            wr = [d(a) for a in wr_np]
+            x = d(x_np.view(np.int16)).view(torch.float16)
+            ib = torch.empty((ncols, 8), dtype=torch.int32, device="cuda")
+            rb = torch.empty((ncols, 8), dtype=torch.float32, device="cuda")
+            for a in wr:
+                calls.append(lambda s, a=a: qg.qmoe_router(a, x, 8, ib, rb, stream=s))
+            wbytes = E * hid * 4  # f32 router weights
+
+            def o_router(i=0):
+                lg, _ = oracle.router_logits(wr_np[i], x_np)
+                _, v = oracle.topk(lg.astype(np.float32), 8)
+                return [oracle.softmax(r) for r in v]
+            o_frac = 1.0
+            o_fn = {t: o_router for t in (1, ncores)}
+            extra = {"bytes_are": "f32 router weights", "topk": 8}
         elif kind == "moe":
             m = synth.moe_layer(ncols, seed=2)
             dm = {}

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemm.so")
 
 EXPORTS = ("qg_status_str", "qgemv_q4_0", "qgemv_q8_0", "qgemm_cols", "qffn_gate_up_silu",
            "qmoe_workspace_bytes", "qmoe_experts", "qmoe_experts_noalloc", "qrepack",
-           "qargmax_f32", "qtopk_f32", "qg_kernel_launches")
+           "qargmax_f32", "qtopk_f32", "qmoe_router", "qg_kernel_launches")
 
 QG_MOE_NOALLOC_WS_BYTES = 8 << 20
 
@@ -68,6 +68,7 @@ def load(path: str | None = None):
     L.qrepack.argtypes = [i32, vp, i32, i32, vp, vp, vp]
     L.qargmax_f32.argtypes = [vp, i32, i32, vp, vp, vp]
     L.qtopk_f32.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+    L.qmoe_router.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
     L.qg_kernel_launches.argtypes = []
     L.qg_kernel_launches.restype = C.c_uint64
     for f in EXPORTS:
@@ -183,3 +184,13 @@ def qtopk_f32(x, k, idx_out, val_out=None, stream=None):
     ncols, n = x.shape
     _check("qtopk_f32", load().qtopk_f32(_ptr(x), n, ncols, int(k), _ptr(idx_out), _ptr(val_out),
                                          _stream(stream)))
+
+
+def qmoe_router(w_router, x, topk, ids_out, rw_out, logits_out=None, stream=None):
+    """MoE router: w_router f32 [n_expert, hidden], x f16 [ncols, hidden] ->
+    ids_out int32 [ncols, topk] (largest logits, lowest id on ties), rw_out f32
+    [ncols, topk] (softmax over them), logits_out None or f32 [ncols, n_expert]."""
+    n_expert, hidden = w_router.shape
+    _check("qmoe_router", load().qmoe_router(_ptr(w_router), _ptr(x), n_expert, hidden, x.shape[0],
+                                             int(topk), _ptr(logits_out), _ptr(ids_out),
+                                             _ptr(rw_out), _stream(stream)))

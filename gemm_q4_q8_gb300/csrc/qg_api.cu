@@ -193,6 +193,20 @@ qg_status qmoe_experts(qg_type t, const void* qg, const uint16_t* sg, const void
   return from_cuda(qg::moe_forward(a, stream));
 }
 
+qg_status qmoe_router(const float* w_router, const uint16_t* x, int n_expert, int hidden,
+                      int ncols, int topk, float* logits_out, int32_t* ids_out, float* rw_out,
+                      cudaStream_t stream) {
+  if (!qg::router_shape_ok(n_expert, hidden, ncols, topk)) return QG_ERR_SHAPE;
+  if (!w_router || !x || !ids_out || !rw_out) return QG_ERR_NULL;
+  if (!aligned(w_router, 16) || !aligned(x, 2) || !aligned(ids_out, 4) || !aligned(rw_out, 4) ||
+      (logits_out && !aligned(logits_out, 4)))
+    return QG_ERR_ALIGN;
+  qg_status st = check_device();
+  if (st != QG_OK) return st;
+  return from_cuda(qg::router_launch(w_router, x, n_expert, hidden, ncols, topk, logits_out,
+                                     ids_out, rw_out, stream));
+}
+
 qg_status qargmax_f32(const float* x, int n, int ncols, int32_t* idx_out, float* val_out,
                       cudaStream_t stream) {
   if (n < 1 || ncols < 1 || ncols > 64) return QG_ERR_SHAPE;

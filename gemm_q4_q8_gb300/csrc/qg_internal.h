@@ -97,4 +97,9 @@ cudaError_t argmax_launch(const float* x, int n, int ncols, int32_t* idx, float*
 cudaError_t topk_launch(const float* x, int n, int ncols, int k, int32_t* idx, float* val,
                         cudaStream_t s);
 
+// MoE router: logits, top-k ids and softmax weights (qg_router.cu).
+bool router_shape_ok(int E, int hidden, int ncols, int topk);
+cudaError_t router_launch(const float* w, const uint16_t* x, int E, int hidden, int ncols,
+                          int topk, float* logits, int32_t* ids, float* rw, cudaStream_t s);
+
 }  // namespace qg

@@ -202,6 +202,21 @@ qg_status qrepack(qg_type t, const void *gguf, int rows, int k, void *q_out,
                   uint16_t *scl_out, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * MoE router ("Engine and kernels", section "Kernel families": router and top-k
+ * on the GPU, so routing needs no readback; the output feeds qmoe_experts).
+ *   w_router   : f32 [n_expert][hidden] (16-byte aligned), 1 <= n_expert <= 1024
+ *   x          : f16 [ncols][hidden], 1 <= ncols <= 16 (the MoE input)
+ *   topk       : 1..32, <= n_expert
+ *   logits_out : NULL or f32 [ncols][n_expert]: logits = W_router x (f32)
+ *   ids_out    : int32 [ncols][topk]: the topk largest logits of each column in
+ *                the qargmax_f32 order (lowest expert id on ties)
+ *   rw_out     : f32 [ncols][topk]: softmax over those topk logits
+ * ------------------------------------------------------------------------- */
+qg_status qmoe_router(const float *w_router, const uint16_t *x, int n_expert, int hidden,
+                      int ncols, int topk, float *logits_out, int32_t *ids_out, float *rw_out,
+                      cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Sampling over f32 logits ("Engine and kernels", section "Kernel families":
  * greedy argmax and top-k on the GPU, so a token reads back a few bytes instead
  * of the logits; section "Fewer passes": lowest-index tie-breaking).

@@ -138,3 +138,24 @@ def test_sampling_argument_errors(lib):
     assert lib.qtopk_f32(ALIGNED, 1000, 1, 257, ALIGNED, None, None) == 2
     assert lib.qtopk_f32(ALIGNED, 1000, 1, 0, ALIGNED, None, None) == 2
     assert lib.qtopk_f32(ALIGNED, 1000, 1, 5, None, None, None) == 1
+
+
+def test_router_argument_errors(lib):
+    def router(w=ALIGNED, x=ALIGNED, E=256, hidden=2048, ncols=1, topk=8, lg=None, ids=ALIGNED,
+               rw=ALIGNED):
+        return lib.qmoe_router(w, x, E, hidden, ncols, topk, lg, ids, rw, None)
+    assert router(E=0) == 2
+    assert router(E=1025) == 2
+    assert router(ncols=17) == 2
+    assert router(topk=33, E=64) == 2
+    assert router(topk=9, E=8) == 2
+    assert router(hidden=0) == 2
+    assert router(w=None) == 1
+    assert router(ids=None) == 1
+    assert router(rw=None) == 1
+    assert router(w=ALIGNED + 4) == 3
+    assert router(x=ALIGNED + 1) == 3
+    assert router(lg=ALIGNED + 2) == 3
+    from conftest import gpu_available
+    if not gpu_available():
+        assert router() == 6
