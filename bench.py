@@ -408,6 +408,7 @@ CONFIGS = (
     ("q4_ffn_down_5120x17408_c16_y0", "cols", synth.Q4_0, 5120, 17408, 16, True),
     ("q8_moe_c1", "moe", synth.Q8_0, 0, 0, 1, False),
     ("q8_moe_c8", "moe", synth.Q8_0, 0, 0, 8, False),
+    ("q8_moe_c16", "moe", synth.Q8_0, 0, 0, 16, False),
     # sampling over LM-head logits (next steps after the LM head): rows = n, k = top-k
     ("argmax_lmhead_248320_c1", "argmax", None, 248320, 1, 1, False),
     ("argmax_lmhead_248320_c8", "argmax", None, 248320, 1, 8, False),

@@ -139,7 +139,8 @@ qg_status qffn_gate_up_silu(qg_type t, const void* qg, const uint16_t* sg, const
 }
 
 size_t qmoe_workspace_bytes(int n_expert, int ffn, int hidden, int ncols, int topk) {
-  if (n_expert < 1 || ffn <= 0 || hidden <= 0 || ncols < 1 || ncols > 8 || topk < 1 || topk > 16)
+  if (n_expert < 1 || n_expert > QG_MOE_MAX_EXPERTS || ffn <= 0 || hidden <= 0 || ncols < 1 ||
+      ncols > 16 || topk < 1 || topk > 16)
     return 0;
   return qg::moe_ws_bytes(n_expert, ffn, hidden, ncols, topk);
 }
@@ -152,8 +153,8 @@ qg_status qmoe_experts(qg_type t, const void* qg, const uint16_t* sg, const void
                        void* ws, size_t ws_bytes, int32_t* err_flag,
                        int32_t* uniq_ids_out, cudaStream_t stream) {
   if (!valid_type((int)t)) return QG_ERR_TYPE;
-  if (n_expert < 1 || ffn <= 0 || hidden <= 0 || (ffn % 32) || (hidden % 32) || ncols < 1 ||
-      ncols > 8 || topk < 1 || topk > 16 || !qg::moe_shape_supported(ffn, hidden, ncols, topk))
+  if (n_expert < 1 || n_expert > QG_MOE_MAX_EXPERTS || ffn <= 0 || hidden <= 0 || (ffn % 32) ||
+      (hidden % 32) || ncols < 1 || ncols > 16 || topk < 1 || topk > 16 || !qg::moe_shape_supported(ffn, hidden, ncols, topk))
     return QG_ERR_SHAPE;
   if (!qg || !sg || !qu || !su || !qd || !sd || !ids || !rw || !x || !y) return QG_ERR_NULL;
   const void* p16[] = {qg, sg, qu, su, qd, sd, x};

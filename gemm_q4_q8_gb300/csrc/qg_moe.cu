@@ -36,9 +36,11 @@ namespace qg {
 constexpr int MOE_WARPS = 8;
 constexpr int MOE_THREADS = MOE_WARPS * 32;
 constexpr int MOE_RW1 = 2;                 // gate/up rows per warp item
-constexpr int MOE_MAXN = 128;              // ncols * topk
+constexpr int MOE_MAXN = 256;              // ncols * topk (16 columns x top-16)
+constexpr int MOE_MAXC = 16;               // columns
 constexpr int MOE_MAXJ = 17;               // topk + shared
-constexpr int MOE_XSMEM_FLOATS = 24576;    // staged activations per CTA (96 KB)
+constexpr int MOE_XSMEM_FLOATS = 32768;    // staged activations per CTA (128 KB)
+static_assert(MOE_MAXN <= MOE_THREADS, "one id-list slot per thread");
 
 struct MoeDev {
   const uint8_t *qg, *qu, *qd;
@@ -113,9 +115,9 @@ __device__ __forceinline__ MoeK1Rows<QT> moe_k1_rows(const MoeDev& p, const int1
 template <int QT>
 __global__ void __launch_bounds__(MOE_THREADS, 2) moe_gate_up_kernel(const MoeDev p) {
   __shared__ int s_ids[MOE_MAXN];
-  __shared__ __align__(16) int s_key[MOE_MAXN];   // id * 128 + position, or INT_MAX
-  __shared__ int16_t s_order[MOE_MAXN + 8];
-  __shared__ int8_t s_pc[MOE_MAXN + 8], s_pj[MOE_MAXN + 8];  // column and k slot of each pair
+  __shared__ __align__(16) int s_key[MOE_MAXN];   // id * MOE_MAXN + position, or INT_MAX
+  __shared__ int16_t s_order[MOE_MAXN + MOE_MAXC];   // routed pairs, then the shared expert's
+  __shared__ int8_t s_pc[MOE_MAXN + MOE_MAXC], s_pj[MOE_MAXN + MOE_MAXC];  // column, k slot
   extern __shared__ float4 smem_f4[];
   float* xs = reinterpret_cast<float*>(smem_f4);
   constexpr int QB = QTraits<QT>::QB;
@@ -330,7 +332,8 @@ size_t moe_ws_bytes(int n_expert, int ffn, int hidden, int ncols, int topk) {
 }
 
 bool moe_shape_supported(int ffn, int hidden, int ncols, int topk) {
-  return (size_t)ncols * hidden <= MOE_XSMEM_FLOATS &&
+  return ncols >= 1 && ncols <= MOE_MAXC && ncols * topk <= MOE_MAXN &&
+         (size_t)ncols * hidden <= MOE_XSMEM_FLOATS &&
          (size_t)(topk + 1) * ffn <= MOE_XSMEM_FLOATS;
 }
 

@@ -127,11 +127,12 @@ qg_status qffn_gate_up_silu(qg_type t, const void *qg, const uint16_t *sg, const
  *
  *   gate/up stacks : [n_expert][ffn][hidden] (quants qg/qu, scales sg/su)
  *   down stack     : [n_expert][hidden][ffn] (quants qd, scales sd)
- *   ids            : device int32 [ncols][topk] expert ids (1 <= topk <= 16)
+ *   ids            : device int32 [ncols][topk] expert ids (1 <= topk <= 16;
+ *                    1 <= n_expert <= QG_MOE_MAX_EXPERTS)
  *   rw             : device f32   [ncols][topk] routing weights
  *   shared         : HOST pointer to a qg_expert of device pointers (one more
  *                    expert of the same shape, added with weight 1), or NULL
- *   x              : f16 [ncols][hidden], 1 <= ncols <= 8
+ *   x              : f16 [ncols][hidden], 1 <= ncols <= 16
  *   y              : f32 [ncols][hidden] =
  *                    y0 + sum_j rw[c][j] * D_e (SiLU(G_e x_c) * (U_e x_c)) + shared,
  *                    e = ids[c][j]; the intermediate h is rounded to f16.
@@ -155,6 +156,7 @@ typedef struct qg_expert {
 } qg_expert;
 
 #define QG_MOE_BAD_ID 1
+#define QG_MOE_MAX_EXPERTS (1 << 22)
 
 size_t qmoe_workspace_bytes(int n_expert, int ffn, int hidden, int ncols, int topk);
 

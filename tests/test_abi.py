@@ -99,7 +99,9 @@ def test_empty_problem_is_ok(lib):
 def test_moe_argument_errors(lib):
     w = lib.qmoe_workspace_bytes(256, 512, 2048, 8, 8)
     assert w > 0
-    assert lib.qmoe_workspace_bytes(256, 512, 2048, 9, 8) == 0
+    assert lib.qmoe_workspace_bytes(256, 512, 2048, 16, 16) > 0
+    assert lib.qmoe_workspace_bytes(256, 512, 2048, 17, 8) == 0
+    assert lib.qmoe_workspace_bytes((1 << 22) + 1, 512, 2048, 1, 8) == 0
 
     def moe(**kw):
         a = dict(t=8, n_expert=4, ffn=64, hidden=64, topk=2, ncols=2, ws=ALIGNED, wsb=1 << 30,
@@ -110,7 +112,8 @@ def test_moe_argument_errors(lib):
                                 None, ALIGNED, a["ncols"], None, a["y"], a["ws"], a["wsb"], None,
                                 None, None)
     assert moe(t=5) == 4
-    assert moe(ncols=9) == 2
+    assert moe(ncols=17) == 2
+    assert moe(n_expert=(1 << 22) + 1) == 2
     assert moe(topk=0) == 2
     assert moe(topk=17) == 2
     assert moe(n_expert=0) == 2

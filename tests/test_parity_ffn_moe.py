@@ -118,7 +118,7 @@ def check_moe(case, ids=None, what=""):
     return y, nu
 
 
-@pytest.mark.parametrize("ncols", [1, 8])
+@pytest.mark.parametrize("ncols", [1, 8, 16])
 def test_moe_layer(ncols):
     case = synth.moe_layer(ncols)
     y, nu = check_moe(case, what=f"MoE 256x top-8 + shared, C={ncols}")
@@ -138,6 +138,13 @@ def test_moe_duplicate_and_invalid_ids():
     ids[2, 0] = -1                 # negative
     ids[3, :] = ids[2, :]
     check_moe(case, ids=ids, what="MoE duplicates + invalid ids")
+
+
+def test_moe_16_columns_top16():
+    """The largest id list: 16 columns x top-16 = 256 slots, many shared experts."""
+    case = synth.moe_case(synth.Q4_0, 40, 96, 256, 16, topk=16, shared=True, residual=True, seed=6)
+    y, nu = check_moe(case, what="MoE 16 columns x top-16")
+    assert nu == len(np.unique(case["ids"]))
 
 
 def test_moe_topk_one_and_all_experts_shared():
