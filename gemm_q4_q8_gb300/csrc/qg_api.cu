@@ -5,6 +5,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <unordered_map>
 
 #include "qg_internal.h"
 #include "qgemm.h"
@@ -27,6 +28,21 @@ int device_sm_count() {
 
 static std::atomic<uint64_t> g_launches{0};
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+bool pdl_allowed(cudaStream_t s, LaunchClass cls) {
+  static std::mutex mu;
+  static std::unordered_map<cudaStream_t, int> last;  // class of the latest launch per stream
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = last.find(s);
+  const int prev = it == last.end() ? -1 : it->second;
+  if (it == last.end()) {
+    if (last.size() > 4096) last.clear();  // streams come and go; forget stale handles
+    last.emplace(s, (int)cls);
+  } else {
+    it->second = (int)cls;
+  }
+  return !(cls == LC_L1 && prev == LC_SMEM);
+}
 
 }  // namespace qg
 

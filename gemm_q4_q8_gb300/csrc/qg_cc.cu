@@ -206,8 +206,11 @@ template <int QT, int NC, int RW, bool DUAL, int EPI>
 static cudaError_t launch_cc_t(const CCParams& p0, cudaStream_t s, int* nlaunch) {
   CCParams p = p0;
   const int nb = p.k / QK;
+  // x chunks of a multiple of 32 blocks keep lane l on blocks l, l+32, ... in
+  // every chunk, as in the 1-column kernel (bit-identical columns)
   int cb = CC_XSMEM_FLOATS / (NC * QK);
-  if (cb > nb) cb = nb;
+  if (cb >= nb) cb = nb;
+  else cb &= ~31;
   p.cb = cb;
   const size_t smem = (size_t)NC * cb * QK * sizeof(float);
   auto kern = qmv_cc_kernel<QT, NC, RW, DUAL, EPI>;
@@ -227,7 +230,7 @@ static cudaError_t launch_cc_t(const CCParams& p0, cudaStream_t s, int* nlaunch)
   if (grid > maxgrid) grid = maxgrid;
   if (grid < 1) grid = 1;
   if (nlaunch) ++*nlaunch;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(CC_THREADS), smem, s, 0, p);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(CC_THREADS), smem, s, 0, LC_L1, p);
 }
 
 template <int QT, bool DUAL, int EPI>

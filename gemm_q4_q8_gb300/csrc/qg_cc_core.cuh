@@ -46,8 +46,10 @@ __device__ __forceinline__ float blk_dot(const Blk<T_Q8_0>& q, const float2 (&xr
   return acc.x + acc.y;
 }
 
-// Dequantised block (for the multi-column baseline: dequantise once, reuse for
-// every column).
+// Dequantised block (for the multi-column kernel: dequantise once, reuse for
+// every column). wv_dot then multiplies and adds in exactly the order of
+// blk_dot (one packed accumulator, elements in order), so a column's block sum
+// is bit-identical to the 1-column kernel's.
 __device__ __forceinline__ void blk_dequant(const Blk<T_Q4_0>& q, float2 (&wv)[16]) {
   const uint32_t w[4] = {q.a.x, q.a.y, q.a.z, q.a.w};
 #pragma unroll
@@ -65,13 +67,10 @@ __device__ __forceinline__ void blk_dequant(const Blk<T_Q8_0>& q, float2 (&wv)[1
   }
 }
 __device__ __forceinline__ float wv_dot(const float2 (&wv)[16], const float2 (&xr)[16]) {
-  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+  float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    a0 = fma2(wv[i], xr[i], a0);
-    a1 = fma2(wv[i + 1], xr[i + 1], a1);
-  }
-  return (a0.x + a0.y) + (a1.x + a1.y);
+  for (int i = 0; i < 16; ++i) acc = fma2(wv[i], xr[i], acc);
+  return acc.x + acc.y;
 }
 
 // Staged x layout of one column: 8 planes of `plane` float4 each; float4 j of

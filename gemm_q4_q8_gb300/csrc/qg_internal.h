@@ -18,12 +18,28 @@ int device_sm_count();
 // Count one kernel launch (see qg_kernel_launches).
 void note_launch(int n = 1);
 
-// Launch `kern` with programmatic stream serialisation (the kernel may begin
-// while the previous kernel on `s` finishes; see pdl_wait in qg_common.cuh),
-// plus a cluster of `cluster_x` CTAs along x when cluster_x > 0.
+// Launch classes for programmatic dependent launch. LC_SMEM: the tensor-core
+// GEMM, whose CTAs hold most of the SM's shared memory and trigger their
+// dependents as soon as they start. LC_L1: every other kernel; they stream
+// through L1 (in-flight loads are staged there) and lose up to a third of
+// their bandwidth if they start on an SM while an LC_SMEM CTA is resident,
+// because a CTA inherits the carve-out of the SM it lands on for its whole
+// life. So an LC_L1 kernel that directly follows an LC_SMEM kernel on the
+// same stream is launched without the programmatic attribute (it starts when
+// that grid completes); every other pair overlaps.
+enum LaunchClass { LC_L1 = 0, LC_SMEM = 1 };
+
+// Records `cls` as the class of the latest launch on `s` and returns whether
+// this launch may use programmatic stream serialisation.
+bool pdl_allowed(cudaStream_t s, LaunchClass cls);
+
+// Launch `kern` on `s` (with programmatic stream serialisation when
+// pdl_allowed says so: the kernel may begin while the previous kernel on `s`
+// finishes; see pdl_wait in qg_common.cuh), plus a cluster of `cluster_x`
+// CTAs along x when cluster_x > 0.
 template <class... KArgs, class... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t s, int cluster_x, Args&&... args) {
+                       cudaStream_t s, int cluster_x, LaunchClass cls, Args&&... args) {
   cudaLaunchConfig_t lc{};
   lc.gridDim = grid;
   lc.blockDim = block;
@@ -31,9 +47,11 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   lc.stream = s;
   cudaLaunchAttribute at[2];
   int na = 0;
-  at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[na].val.programmaticStreamSerializationAllowed = 1;
-  ++na;
+  if (pdl_allowed(s, cls)) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   if (cluster_x > 0) {
     at[na].id = cudaLaunchAttributeClusterDimension;
     at[na].val.clusterDim.x = (unsigned)cluster_x;

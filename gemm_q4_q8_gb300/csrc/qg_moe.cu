@@ -350,7 +350,7 @@ static cudaError_t launch_moe(K kern, long grid_max_units, int multiple, size_t 
   if (grid > grid_max_units) grid = grid_max_units;
   grid = grid / multiple * multiple;
   if (grid < multiple) grid = multiple;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(MOE_THREADS), smem, s, 0, d);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(MOE_THREADS), smem, s, 0, LC_L1, d);
 }
 
 template <int QT>

@@ -228,7 +228,7 @@ static cudaError_t router_go(size_t smem, const float* w, const __half* x, int E
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(RT_CLUSTER), dim3(RT_THREADS), smem, s, RT_CLUSTER, w, x, E,
+  return launch_pdl(kern, dim3(RT_CLUSTER), dim3(RT_THREADS), smem, s, RT_CLUSTER, LC_L1, w, x, E,
                     hidden, ncols, topk, logits, ids, rw);
 }
 
@@ -238,8 +238,11 @@ cudaError_t router_launch(const float* w, const uint16_t* x, int E, int hidden, 
   const size_t s_x = (size_t)ncols * hidden * 2;
   const bool xs = s_x <= RT_XS_MAX;
   // float4 rows need 16-byte row starts (w itself is 16-byte aligned) and
-  // 8-byte x row starts (always, when x is staged in shared memory)
-  const bool vec = (hidden % 4) == 0 && (xs || (reinterpret_cast<uintptr_t>(x) & 7) == 0);
+  // 8-byte x row starts. The choice depends on the pointers and hidden only,
+  // never on the column count, so a column's logit is the same bit for bit
+  // whatever the number of columns (the lane -> k order differs between the
+  // float4 and scalar sweeps).
+  const bool vec = (hidden % 4) == 0 && (reinterpret_cast<uintptr_t>(x) & 7) == 0;
   if (xs && vec) {
     if (ncols == 1) return router_go<1, true, true>(s_x, w, xh, E, hidden, ncols, topk, logits, ids, rw, s);
     if (ncols <= 2) return router_go<2, true, true>(s_x, w, xh, E, hidden, ncols, topk, logits, ids, rw, s);

@@ -254,7 +254,7 @@ cudaError_t argmax_launch(const float* x, int n, int ncols, int32_t* idx, float*
   cudaError_t e = cudaFuncSetAttribute(argmax_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   return launch_pdl(argmax_kernel, dim3((unsigned)(ncols * AMX_CLUSTER)), dim3(SMP_THREADS), 0, s,
-                    AMX_CLUSTER, x, n, idx, val);
+                    AMX_CLUSTER, LC_L1, x, n, idx, val);
 }
 
 cudaError_t topk_launch(const float* x, int n, int ncols, int k, int32_t* idx, float* val,
@@ -264,7 +264,7 @@ cudaError_t topk_launch(const float* x, int n, int ncols, int k, int32_t* idx, f
                                        (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(topk_kernel, dim3((unsigned)(ncols * SMP_CLUSTER)), dim3(SMP_THREADS), smem,
-                    s, SMP_CLUSTER, x, n, k, idx, val);
+                    s, SMP_CLUSTER, LC_L1, x, n, k, idx, val);
 }
 
 }  // namespace qg

@@ -232,10 +232,12 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   __syncthreads();
 
   const bool producer = warp == TC_WARP_TMA;
-  // No early trigger here: a kernel that starts on an SM while this kernel's
-  // CTAs are resident inherits their shared-memory carve-out, and the
-  // CUDA-core kernels stream far slower with that little L1 left. Dependents
-  // launch when this grid completes.
+  // Dependents may launch at once: another tensor-core GEMM queues its CTAs
+  // behind this grid's and issues its first weight loads as soon as it lands.
+  // The host never lets a CUDA-core kernel follow this one programmatically
+  // (LC_SMEM -> LC_L1 in launch_pdl): it would inherit this kernel's
+  // shared-memory carve-out and stream far slower with that little L1 left.
+  pdl_trigger();
   if (producer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
@@ -639,19 +641,23 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
   const int ntile = (rows + TC_BM - 1) / TC_BM;
   (void)S::NF;
   return launch_pdl(kern, dim3((unsigned)(ntile * cfg.ksplit)), dim3(TC_THREADS), cfg.smem, s,
-                    cfg.ksplit, mA0, mS0, mA1, mS1, mX, p);
+                    cfg.ksplit, LC_SMEM, mA0, mS0, mA1, mS1, mX, p);
 }
 
 }  // namespace
 
-// Shapes the tensor-core plan takes: 2-16 columns, and one column of a large
-// Q4_0 matrix (from 16,384 rows the f16 dequantisation of the mma path costs
-// fewer instructions per weight than the f32 CUDA-core dot, and the wider
-// tile stream wins: measured 4.6 -> 5.4 TB/s on 248,320 x 5120; Q8_0 and
-// smaller matrices stay on the CUDA-core GEMV, which is as fast or faster).
+// Shapes the tensor-core plan takes: K a multiple of 256, any column count
+// from 1 to 16, except that matrices of at most 2^22 weights with K <= 3072
+// keep 1-8 columns on the CUDA cores (their fixed latency is lower there:
+// 2048 x 2048 Q8_0 takes 4.1 us on CUDA cores and 6.8 us here at 1 column,
+// 7.5 and 6.8 us at 8). For 1-8 columns the choice depends on the matrix only,
+// and the plan is the same (one n-tile of 8), so the 1-column GEMV and its
+// 2-8-column twins give bit-identical columns: the mma computes each output
+// column from that column alone, and the CUDA-core twins repeat the 1-column
+// arithmetic column by column.
 bool tc_supported(int qt, int ncols, bool dual, int rows, int k) {
-  if (ncols == 1 && !(qt == T_Q4_0 && !dual && rows >= 16384)) return false;
   if (k <= 0 || k % TC_KT != 0 || ncols < 1 || ncols > 16 || rows <= 0) return false;
+  if (ncols <= 8 && (long long)rows * k <= (1LL << 22) && k <= 3072) return false;
   const bool wide = ncols > 8;
   if (qt == T_Q4_0) {
     if (dual) return wide ? config_ok<T_Q4_0, 2, true>(rows, k) : config_ok<T_Q4_0, 1, true>(rows, k);
