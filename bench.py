@@ -398,12 +398,14 @@ CONFIGS = (
     ("q8_gemv_2048_c1", "gemv", synth.Q8_0, 2048, 2048, 1, False),
     ("q4_gemv_5120_c1_y0", "gemv", synth.Q4_0, 5120, 5120, 1, True),
     ("q8_lmhead_248320_c1", "gemv", synth.Q8_0, 248320, 5120, 1, False),
+    ("q4_lmhead_248320_c1", "gemv", synth.Q4_0, 248320, 5120, 1, False),
     ("q4_twins_5120_c2", "gemv", synth.Q4_0, 5120, 5120, 2, False),
     ("q4_twins_5120_c4", "gemv", synth.Q4_0, 5120, 5120, 4, False),
     ("q4_twins_5120_c8", "gemv", synth.Q4_0, 5120, 5120, 8, False),
     ("q4_twins_17408_c2", "gemv", synth.Q4_0, 17408, 5120, 2, False),
     ("q4_twins_17408_c4", "gemv", synth.Q4_0, 17408, 5120, 4, False),
     ("q4_twins_17408_c8", "gemv", synth.Q4_0, 17408, 5120, 8, False),
+    ("q8_twins_17408_c8", "gemv", synth.Q8_0, 17408, 5120, 8, False),
     ("q4_ffn_gateup_17408_c16", "gateup", synth.Q4_0, 17408, 5120, 16, False),
     ("q4_ffn_down_5120x17408_c16_y0", "cols", synth.Q4_0, 5120, 17408, 16, True),
     ("q8_moe_c1", "moe", synth.Q8_0, 0, 0, 1, False),

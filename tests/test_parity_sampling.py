@@ -42,6 +42,11 @@ def logits(n, ncols, seed, kind):
         x = np.tile(np.arange(n, dtype=np.float32), (ncols, 1))
     elif kind == "allnan":
         x = np.full((ncols, n), np.nan, dtype=np.float32)
+    elif kind.startswith("lanes"):  # the largest values on a few index classes mod 512:
+        m = int(kind[5:])          # many keys clear the threshold of thread maxima
+        x = g.standard_normal((ncols, n)).astype(np.float32)
+        big = (np.arange(n) % 512) < m
+        x[:, big] += 1000.0
     return x
 
 
@@ -72,6 +77,13 @@ def test_lm_head_width(kind):
                                        (65536, 1, 64), (33333, 4, 17)])
 def test_ragged_shapes(n, ncols, k):
     check(logits(n, ncols, n + k, "ties"), k)
+
+
+@pytest.mark.parametrize("m,k", [(64, 64), (256, 256), (16, 40)])
+def test_many_candidates(m, k):
+    """Index classes that hold every large value: k = 64 leaves ~2,000 keys
+    above the threshold (sorted), k = 256 ~7,800 (the streaming fallback)."""
+    check(logits(248320, 2, 5, f"lanes{m}"), k)
 
 
 def test_all_nan_and_ascending():
