@@ -145,6 +145,8 @@ __device__ __forceinline__ void cc_rowdot_1col(const uint8_t* __restrict__ qa,
                                                const float* xs, int plane, int kb0, int kb1,
                                                int lane, float (&ta)[RW], float (&tb)[RW]) {
   constexpr int QB = QTraits<QT>::QB;
+  // two blocks per lane in flight: a 2048-wide row is one round trip, not two
+#pragma unroll 2
   for (int b = kb0 + lane; b < kb1; b += 32) {
     Blk<QT> bqa[RW], bqb[RW];
     uint16_t bsa[RW], bsb[RW];

@@ -112,8 +112,10 @@ __device__ __forceinline__ MoeK1Rows<QT> moe_k1_rows(const MoeDev& p, const int1
   return w;
 }
 
-template <int QT>
-__global__ void __launch_bounds__(MOE_THREADS, 2) moe_gate_up_kernel(const MoeDev p) {
+// WARPS: 8, or 16 when the staged x is too large for two CTAs per SM (one
+// CTA of 16 warps then keeps as many rows in flight as two of 8).
+template <int QT, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) moe_gate_up_kernel(const MoeDev p) {
   __shared__ int s_ids[MOE_MAXN];
   __shared__ __align__(16) int s_key[MOE_MAXN];   // id * MOE_MAXN + position, or INT_MAX
   __shared__ int16_t s_order[MOE_MAXN + MOE_MAXC];   // routed pairs, then the shared expert's
@@ -187,8 +189,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_gate_up_kernel(const MoeDe
   const size_t mat_s = (size_t)p.ffn * nb;
   const int ngroups = (p.ffn + MOE_RW1 - 1) / MOE_RW1;
   const int total = P * ngroups;
-  const int stride = gridDim.x * MOE_WARPS;
-  int item = blockIdx.x * MOE_WARPS + warp;
+  const int stride = gridDim.x * WARPS;
+  int item = blockIdx.x * WARPS + warp;
 
   stage_x_cols(QT, xs, k, p.x, (size_t)k, p.ncols, k);
   __syncthreads();
@@ -338,35 +340,39 @@ bool moe_shape_supported(int ffn, int hidden, int ncols, int topk) {
 }
 
 template <class K>
-static cudaError_t launch_moe(K kern, long grid_max_units, int multiple, size_t smem,
+static cudaError_t launch_moe(K kern, int threads, long grid_max_units, int multiple, size_t smem,
                               const MoeDev& d, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int occ = 1;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, MOE_THREADS, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
   if (e != cudaSuccess) return e;
   if (occ < 1) occ = 1;
   long grid = (long)device_sm_count() * occ;
   if (grid > grid_max_units) grid = grid_max_units;
   grid = grid / multiple * multiple;
   if (grid < multiple) grid = multiple;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(MOE_THREADS), smem, s, 0, LC_L1, d);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3((unsigned)threads), smem, s, 0, LC_L1, d);
 }
 
 template <int QT>
 static cudaError_t moe_launch_t(const MoeDev& d, cudaStream_t s) {
   const int ngroups = (d.ffn + MOE_RW1 - 1) / MOE_RW1;
   const long pairs_max = (long)d.ncols * d.topk + (d.has_shared ? d.ncols : 0);
-  const long ctas_gu = (pairs_max * ngroups + MOE_WARPS - 1) / MOE_WARPS;
-  cudaError_t e = launch_moe(moe_gate_up_kernel<QT>, ctas_gu, 1,
-                             (size_t)d.ncols * d.hidden * sizeof(float), d, s);
+  const size_t smem_gu = (size_t)d.ncols * d.hidden * sizeof(float);
+  cudaError_t e;
+  if (smem_gu <= 100 * 1024) {
+    e = launch_moe(moe_gate_up_kernel<QT, 8>, 256, (pairs_max * ngroups + 7) / 8, 1, smem_gu, d, s);
+  } else {
+    e = launch_moe(moe_gate_up_kernel<QT, 16>, 512, (pairs_max * ngroups + 15) / 16, 1, smem_gu, d, s);
+  }
   if (e != cudaSuccess) return e;
   const size_t smem_dn = (size_t)(d.topk + 1) * d.ffn * sizeof(float);
   const long big = 1L << 30;
   // one row per lane per item when few columns share the grid (more items,
   // all of a lane's experts in flight at once); two rows otherwise
-  if (d.ncols <= 2) return launch_moe(moe_down_kernel<QT, 1, 9>, big, d.ncols, smem_dn, d, s);
-  return launch_moe(moe_down_kernel<QT, 2, 3>, big, d.ncols, smem_dn, d, s);
+  if (d.ncols <= 2) return launch_moe(moe_down_kernel<QT, 1, 9>, MOE_THREADS, big, d.ncols, smem_dn, d, s);
+  return launch_moe(moe_down_kernel<QT, 2, 3>, MOE_THREADS, big, d.ncols, smem_dn, d, s);
 }
 
 cudaError_t moe_forward(const MoeArgs& a, cudaStream_t s) {
