@@ -78,14 +78,23 @@ def peaks():
 
 
 # --------------------------------------------------------------- workload
-def make_workload(seed: int = 0) -> dict:
-    """All host-side inputs of one step (numpy), drawn once."""
+def make_workload(seed: int = 0, only=None) -> dict:
+    """All host-side inputs of one step (numpy), drawn once; `only` names one
+    call of the step whose inputs alone are drawn (the same values)."""
     w = {}
-    w["gemv"] = synth.q4_gemv_residual(seed)
-    w["lmhead"] = synth.lm_head(seed + 1)
-    w["twins"] = synth.twins(17408, 8, seed + 2)
-    w["ffn"] = synth.prefill_ffn(seed + 3)
-    w["moe"] = synth.moe_layer(8, seed + 4)
+    need = {"gemv": ("gemv",), "lmhead": ("lmhead",), "twins": ("twins",),
+            "gateup": ("ffn",), "down": ("ffn",), "moe": ("moe",)}
+    keep = need.get(only) if only else None
+    if keep is None or "gemv" in keep:
+        w["gemv"] = synth.q4_gemv_residual(seed)
+    if keep is None or "lmhead" in keep:
+        w["lmhead"] = synth.lm_head(seed + 1)
+    if keep is None or "twins" in keep:
+        w["twins"] = synth.twins(17408, 8, seed + 2)
+    if keep is None or "ffn" in keep:
+        w["ffn"] = synth.prefill_ffn(seed + 3)
+    if keep is None or "moe" in keep:
+        w["moe"] = synth.moe_layer(8, seed + 4)
     return w
 
 
@@ -130,7 +139,8 @@ class GpuStep:
         def want(*names):
             return only is None or only in names
 
-        g, l, tw, f, m = w["gemv"], w["lmhead"], w["twins"], w["ffn"], w["moe"]
+        g, l, tw, f, m = (w.get("gemv"), w.get("lmhead"), w.get("twins"), w.get("ffn"),
+                          w.get("moe"))
         if want("gemv"):
             self.g_q, self.g_s = dq(synth.Q4_0, g["q"], g["scl"])
         if want("lmhead"):
@@ -155,32 +165,40 @@ class GpuStep:
             self.m_uniq = t.empty(m["ncols"] * m["topk"], dtype=t.int32, device="cuda")
 
         # per-step inputs (device) and their pinned host copies (for e2e)
-        self.host_in = {
-            "g_x": g["x"].view(np.int16), "g_y0": g["y0"],
-            "l_x": l["x"].view(np.int16),
-            "t_x": tw["x"].view(np.int16),
-            "f_x": f["x"].view(np.int16), "f_y0": f["y0"],
-            "m_x": m["x"].view(np.int16), "m_ids": m["ids"], "m_rw": m["rw"],
-        }
+        self.host_in = {}
+        if g is not None:
+            self.host_in.update({"g_x": g["x"].view(np.int16), "g_y0": g["y0"]})
+        if l is not None:
+            self.host_in["l_x"] = l["x"].view(np.int16)
+        if tw is not None:
+            self.host_in["t_x"] = tw["x"].view(np.int16)
+        if f is not None:
+            self.host_in.update({"f_x": f["x"].view(np.int16), "f_y0": f["y0"]})
+        if m is not None:
+            self.host_in.update({"m_x": m["x"].view(np.int16), "m_ids": m["ids"], "m_rw": m["rw"]})
         self.din = {k: d(v) for k, v in self.host_in.items()}
         self.pin_in = {k: t.from_numpy(np.ascontiguousarray(v)).pin_memory()
                        for k, v in self.host_in.items()}
         f16 = t.float16
-        self.out = {
-            "g_y": t.empty((1, g["scl"].shape[0]), dtype=t.float32, device="cuda"),
-            "l_y": t.empty((1, l["scl"].shape[0]), dtype=t.float32, device="cuda"),
-            "t_y": t.empty((8, tw["scl"].shape[0]), dtype=t.float32, device="cuda"),
-            "f_h": t.empty((16, 17408), dtype=f16, device="cuda"),
-            "f_y": t.empty((16, 5120), dtype=t.float32, device="cuda"),
-            "m_y": t.empty((8, 2048), dtype=t.float32, device="cuda"),
-        }
+        self.out = {}
+        if g is not None:
+            self.out["g_y"] = t.empty((1, g["scl"].shape[0]), dtype=t.float32, device="cuda")
+        if l is not None:
+            self.out["l_y"] = t.empty((1, l["scl"].shape[0]), dtype=t.float32, device="cuda")
+        if tw is not None:
+            self.out["t_y"] = t.empty((8, tw["scl"].shape[0]), dtype=t.float32, device="cuda")
+        if f is not None:
+            self.out["f_h"] = t.empty((16, 17408), dtype=f16, device="cuda")
+            self.out["f_y"] = t.empty((16, 5120), dtype=t.float32, device="cuda")
+        if m is not None:
+            self.out["m_y"] = t.empty((8, 2048), dtype=t.float32, device="cuda")
         self.pin_out = {k: t.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.out.items()}
 
     def x16(self, key):
         return self.din[key].view(self.torch.float16)
 
     def call(self, name: str, stream):
-        qg, o, m = self.qg, self.out, self.w["moe"]
+        qg, o, m = self.qg, self.out, self.w.get("moe")
         if name == "gemv":
             qg.qgemv_q4_0(self.g_q, self.g_s, self.x16("g_x"), o["g_y"], self.din["g_y0"], stream)
         elif name == "lmhead":
@@ -374,9 +392,13 @@ def run_case(args):
     import gemm_q4_q8_gb300 as qg
     from gemm_q4_q8_gb300 import build
     build.build()
-    w = make_workload(0)
+    if args.case in EXTRA_CASES:
+        return run_extra_case(args, torch, qg)
+    w = make_workload(0, only=args.case)
     if args.case_rows:
         for key in ("gemv", "lmhead", "twins"):
+            if key not in w:
+                continue
             c = w[key]
             r = min(args.case_rows, c["scl"].shape[0])
             c["q"], c["scl"] = c["q"][:r], c["scl"][:r]
@@ -387,6 +409,37 @@ def run_case(args):
     stream = torch.cuda.current_stream()
     for _ in range(args.steps):
         gs.call(args.case, stream)
+    torch.cuda.synchronize()
+    print("ok", args.case)
+    return 0
+
+
+# The next steps around the step's calls, as single-kernel profiling targets
+# at their config sizes: greedy argmax and top-40 over one column of 248,320
+# logits; the MoE router (256 x 2048 f32, top-8) on one column.
+EXTRA_CASES = ("argmax", "topk40", "router")
+
+
+def run_extra_case(args, torch, qg):
+    g = synth.rng(11)
+    stream = torch.cuda.current_stream()
+    if args.case in ("argmax", "topk40"):
+        x = torch.from_numpy(g.standard_normal((1, 248320)).astype(np.float32)).cuda()
+        k = 1 if args.case == "argmax" else 40
+        idx = torch.empty((1, k), dtype=torch.int32, device="cuda")
+        val = torch.empty((1, k), dtype=torch.float32, device="cuda")
+        for _ in range(args.steps):
+            if args.case == "argmax":
+                qg.qargmax_f32(x, idx[:, 0], val[:, 0], stream)
+            else:
+                qg.qtopk_f32(x, k, idx, val, stream)
+    else:
+        w = torch.from_numpy((g.standard_normal((256, 2048)) * 0.02).astype(np.float32)).cuda()
+        x = torch.from_numpy(synth.draw_x(g, 1, 2048).view(np.int16)).cuda().view(torch.float16)
+        ids = torch.empty((1, 8), dtype=torch.int32, device="cuda")
+        rw = torch.empty((1, 8), dtype=torch.float32, device="cuda")
+        for _ in range(args.steps):
+            qg.qmoe_router(w, x, 8, ids, rw, stream=stream)
     torch.cuda.synchronize()
     print("ok", args.case)
     return 0
@@ -476,6 +529,7 @@ def run_configs(args):
                 else:
                     calls.append(lambda s, a=a: qg.qtopk_f32(a, kk, ib, vb, s))
             wbytes = ncols * n * 4  # logits read (no weights)
+            tbytes = wbytes + ncols * kk * 8  # + indices and values written
             o_frac = 1.0
             o_fn = {t: ((lambda: oracle.argmax(xs_np[0])) if kind == "argmax"
                         else (lambda: oracle.topk(xs_np[0], kk))) for t in (1, ncores)}
@@ -491,6 +545,7 @@ def run_configs(args):
             for a in wr:
                 calls.append(lambda s, a=a: qg.qmoe_router(a, x, 8, ib, rb, stream=s))
             wbytes = E * hid * 4  # f32 router weights
+            tbytes = wbytes + ncols * hid * 2 + ncols * 8 * 8  # + x, ids and weights out
 
             def o_router(i=0):
                 lg, _ = oracle.router_logits(wr_np[i], x_np)
@@ -514,6 +569,8 @@ def run_configs(args):
                    for _ in range(8)]
             uniq = float(np.mean([len(np.unique(i)) for i in idn]))
             wbytes = (uniq + 1) * 3 * synth.weight_bytes(qt, 512, 2048)
+            # + x, y, ids, rw, and h (f16 [ncols][9][512]) written then read
+            tbytes = wbytes + ncols * 2048 * (2 + 4) + ncols * 8 * 8 + 2 * ncols * 9 * 512 * 2
             ids = [d(i) for i in idn]
             rw, x = d(m["rw"]), d(m["x"].view(np.int16)).view(torch.float16)
             y = torch.empty((ncols, 2048), dtype=torch.float32, device="cuda")
@@ -551,6 +608,9 @@ def run_configs(args):
                     else:
                         calls.append(lambda s, a=a, sa=sa: fn(a, sa, x, y, y0, s))
             wbytes = wb1
+            # + x read, y (f32) or h (f16) written, y0 read
+            out_b = ncols * rows * (2 if kind == "gateup" else 4)
+            tbytes = wbytes + ncols * k * 2 + out_b + (ncols * rows * 4 if residual else 0)
             # the oracle runs on an evenly spaced row sample of about 25 M weights
             # (the whole matrix when it is smaller), its time scaled to all rows
             n_s = max(1, min(rows, int(25e6 / (nmat * k))))
@@ -595,6 +655,7 @@ def run_configs(args):
             "config": name, "us_median": med,
             "us_p10": float(np.percentile(per_call, 10)), "us_p90": float(np.percentile(per_call, 90)),
             "timed_calls": int(nrep * reps), "weight_bytes": wbytes,
+            "total_bytes": tbytes,
             "GBps": wbytes / (med * 1e-6) / 1e9,
             "frac_of_measured_hbm": wbytes / (med * 1e-6) / 1e9 / peak, "peak_kind": peak_kind,
             "frac_of_8TBps_nominal": wbytes / (med * 1e-6) / 8e12,
@@ -650,7 +711,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--ref-frac", type=float, default=1 / 256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=KERNELS, default=None,
+    ap.add_argument("--case", choices=KERNELS + EXTRA_CASES, default=None,
                     help="profiling target: run only this call (see run_case)")
     ap.add_argument("--case-rows", type=int, default=0)
     ap.add_argument("--configs", action="store_true",

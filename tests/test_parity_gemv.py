@@ -70,12 +70,27 @@ def test_q4_gemv_residual_in_place():
     check_case(synth.q4_gemv_residual(seed=1), inplace=True, what="Q4_0 in place y += W x")
 
 
-def test_lm_head_sampled_rows():
+def test_lm_head_all_rows_and_draft_head():
+    """The full 248,320-row Q8_0 LM head against the multithreaded oracle on
+    every row, and the draft head: the same call on the first 65,536 rows of
+    the same weights (a row prefix, no copy)."""
     case = synth.lm_head()
-    g = np.random.Generator(np.random.PCG64(99))
-    sel = np.unique(np.concatenate([np.arange(64), case["rows"] - 64 + np.arange(64),
-                                    g.integers(0, case["rows"], 4096)]))
-    check_case(case, rows_sel=sel, what="Q8_0 LM head 248320x5120 (sampled rows)")
+    qtype, rows = case["qtype"], case["rows"]
+    dq, ds = dev_q(qtype, case["q"], case["scl"])
+    dx = dev_u16_as_f16(case["x"])
+    y = torch.full((1, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qg.qgemv_q8_0(dq, ds, dx, y)
+    nd = 65536
+    yd = torch.full((1, nd), float("nan"), dtype=torch.float32, device="cuda")
+    qg.qgemv_q8_0(dq[:nd], ds[:nd], dx, yd)
+    torch.cuda.synchronize()
+    yr, S = oracle.matmul(qtype, case["q"], case["scl"], case["x"], None, nthreads=NTHREADS)
+    got = host(y)
+    assert np.isfinite(got).all()
+    assert_within(got, yr, gemv_bound(S), "Q8_0 LM head 248320x5120, every row")
+    gd = host(yd)
+    assert np.isfinite(gd).all()
+    assert_within(gd, yr[:, :nd], gemv_bound(S[:, :nd]), "draft head: first 65536 rows")
 
 
 def test_q4_large_one_column_sampled_rows():
