@@ -706,7 +706,9 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    # default: 1000 device steps (~0.3 s timed, several clock samples); the
+    # reference arm's steps are oracle passes of ~0.25 s each, so 20 there
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--ref-frac", type=float, default=1 / 256)
@@ -718,6 +720,8 @@ def main(argv=None):
                     help="time every workload config alone (one JSON line each)")
     ap.add_argument("--config-filter", default="")
     args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = 20 if args.impl == "reference" else (200 if args.case else 1000)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -93,6 +93,22 @@ def test_lm_head_all_rows_and_draft_head():
     assert_within(gd, yr[:, :nd], gemv_bound(S[:, :nd]), "draft head: first 65536 rows")
 
 
+def test_q4_lm_head_shape_all_rows():
+    """One column of a Q4_0 matrix of the LM head's shape (248,320 x 5120, the
+    bench's Q4_0 LM-head config) against the multithreaded oracle on every row;
+    the output starts as NaN, so an unwritten row fails."""
+    rows, k = 248320, 5120
+    case = synth.gemv_case(synth.Q4_0, rows, k, 1, residual=False, seed=43)
+    dq, ds = dev_q(synth.Q4_0, case["q"], case["scl"])
+    y = torch.full((1, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qg.qgemv_q4_0(dq, ds, dev_u16_as_f16(case["x"]), y)
+    torch.cuda.synchronize()
+    yr, S = oracle.matmul(synth.Q4_0, case["q"], case["scl"], case["x"], None, nthreads=NTHREADS)
+    got = host(y)
+    assert np.isfinite(got).all()
+    assert_within(got, yr, gemv_bound(S), "Q4_0 248320x5120 C=1, every row")
+
+
 def test_q4_large_one_column_sampled_rows():
     """One column of a large Q4_0 matrix (the tensor-core plan), ragged row tail."""
     case = synth.gemv_case(synth.Q4_0, 20000, 5120, 1, residual=True, seed=41)
