@@ -384,6 +384,14 @@ def max_over_ranks(v: float, world: int, torch, device) -> float:
     return float(t.item())
 
 
+def whole_job_rate(step_bytes: float, region_ms: float, steps: int, world: int, torch,
+                   device) -> tuple:
+    """(ms per step, GB/s) of the whole job: the slowest rank's timed region
+    sets the step time; every rank streamed `step_bytes` per step."""
+    ms_per_step = max_over_ranks(region_ms, world, torch, device) / steps
+    return ms_per_step, world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
 def run_case(args):
     """Profiling target: one call of the step, `--steps` times back to back, at
     full size or with its matrix cut to `--case-rows` rows; prints nothing but
@@ -796,9 +804,8 @@ def main(argv=None):
     if world > 1:
         torch.distributed.barrier()
     clk.stop()
-    region_ms = e0.elapsed_time(e1)
-    region_ms = max_over_ranks(region_ms, world, torch, device)
-    ms_per_step = region_ms / args.steps
+    ms_per_step, value = whole_job_rate(step_bytes, e0.elapsed_time(e1), args.steps, world,
+                                        torch, device)
 
     # ---- per-kernel breakdown: per-call graphs with events between them
     nb_steps = max(3, min(args.steps, 50))
@@ -842,7 +849,7 @@ def main(argv=None):
 
     line = {
         "metric": METRIC,
-        "value": world * step_bytes / (ms_per_step * 1e-3) / 1e9,
+        "value": value,
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
