@@ -82,93 +82,41 @@ qmv_cc_kernel(const CCParams p) {
   const int iters = gfirst < ngroups ? (ngroups - gfirst + gstride - 1) / gstride : 0;
 
   pdl_trigger();
-  // The first 32 blocks of every row of this CTA's first row groups are pulled
-  // into L2 before waiting for the previous kernel (weights are never written
-  // by it), so the stream starts while that kernel drains and x is staged.
-  if (nchunk == 1 && iters > 0 && threadIdx.x < CC_WARPS * RW) {
-    const int row = gfirst * RW + (int)threadIdx.x;
-    if (row < p.rows) {
-      const int pb = (nb < 32 ? nb : 32) * QB;
-      l2_prefetch_bulk(p.qa + (size_t)row * rowbytes, (uint32_t)pb);
-      l2_prefetch_line(p.sa + (size_t)row * nb);
-      if (DUAL) {
-        l2_prefetch_bulk(p.qb + (size_t)row * rowbytes, (uint32_t)pb);
-        l2_prefetch_line(p.sb + (size_t)row * nb);
+
+  // One block b of the warp's rows, quants and scales already in registers:
+  // per row and column, scale * (block dot) into the row's total, in the same
+  // order for any column count.
+  float ta[RW][NC], tb[RW][NC];
+  auto accumulate = [&](const Blk<QT> (&qa)[RW], const uint16_t (&sa)[RW], const Blk<QT> (&qb)[RW],
+                        const uint16_t (&sb)[RW], int bx) {
+    if (NC == 1) {
+      float2 xr[16];
+      load_x16(xs, cb, bx, xr);
+#pragma unroll
+      for (int r = 0; r < RW; ++r) {
+        ta[r][0] = fmaf(h2f(sa[r]), blk_dot(qa[r], xr), ta[r][0]);
+        if (DUAL) tb[r][0] = fmaf(h2f(sb[r]), blk_dot(qb[r], xr), tb[r][0]);
       }
-    }
-  }
-  pdl_wait();
-
-  if (nchunk == 1) {
-    stage_x<QT, NC>(xs, xstride, p.x, k, cols, 0, nb);
-    __syncthreads();
-  }
-
-  for (int it = 0; it < iters; ++it) {
-    const int g = gfirst + warp + it * gstride;
-    const bool active = g < ngroups;
-    int rowidx[RW];
+    } else {
 #pragma unroll
-    for (int r = 0; r < RW; ++r) rowidx[r] = min(g * RW + r, p.rows - 1);
-
-    float ta[RW][NC], tb[RW][NC];
+      for (int r = 0; r < RW; ++r) {
+        float2 wa[16], wb[16];
+        blk_dequant(qa[r], wa);
+        if (DUAL) blk_dequant(qb[r], wb);
+        const float da = h2f(sa[r]);
+        const float db = DUAL ? h2f(sb[r]) : 0.f;
 #pragma unroll
-    for (int r = 0; r < RW; ++r)
-#pragma unroll
-      for (int c = 0; c < NC; ++c) { ta[r][c] = 0.f; tb[r][c] = 0.f; }
-
-    for (int ch = 0; ch < nchunk; ++ch) {
-      const int kb0 = ch * cb;
-      const int kb1 = min(nb, kb0 + cb);
-      if (nchunk > 1) {
-        __syncthreads();
-        stage_x<QT, NC>(xs, xstride, p.x, k, cols, kb0, kb1);
-        __syncthreads();
-      }
-      if (!active) continue;
-
-      for (int b = kb0 + lane; b < kb1; b += 32) {
-        Blk<QT> qa[RW], qb[RW];
-        uint16_t sa[RW], sb[RW];
-#pragma unroll
-        for (int r = 0; r < RW; ++r) {
-          qa[r].load(p.qa + (size_t)rowidx[r] * rowbytes + (size_t)b * QB);
-          sa[r] = ld_u16(p.sa + (size_t)rowidx[r] * nb + b);
-          if (DUAL) {
-            qb[r].load(p.qb + (size_t)rowidx[r] * rowbytes + (size_t)b * QB);
-            sb[r] = ld_u16(p.sb + (size_t)rowidx[r] * nb + b);
-          }
-        }
-        if (NC == 1) {
+        for (int c = 0; c < NC; ++c) {
           float2 xr[16];
-          load_x16(xs, cb, b - kb0, xr);
-#pragma unroll
-          for (int r = 0; r < RW; ++r) {
-            ta[r][0] = fmaf(h2f(sa[r]), blk_dot(qa[r], xr), ta[r][0]);
-            if (DUAL) tb[r][0] = fmaf(h2f(sb[r]), blk_dot(qb[r], xr), tb[r][0]);
-          }
-        } else {
-#pragma unroll
-          for (int r = 0; r < RW; ++r) {
-            float2 wa[16], wb[16];
-            blk_dequant(qa[r], wa);
-            if (DUAL) blk_dequant(qb[r], wb);
-            const float da = h2f(sa[r]);
-            const float db = DUAL ? h2f(sb[r]) : 0.f;
-#pragma unroll
-            for (int c = 0; c < NC; ++c) {
-              float2 xr[16];
-              load_x16(xs + c * xstride, cb, b - kb0, xr);
-              ta[r][c] = fmaf(da, wv_dot(wa, xr), ta[r][c]);
-              if (DUAL) tb[r][c] = fmaf(db, wv_dot(wb, xr), tb[r][c]);
-            }
-          }
+          load_x16(xs + c * xstride, cb, bx, xr);
+          ta[r][c] = fmaf(da, wv_dot(wa, xr), ta[r][c]);
+          if (DUAL) tb[r][c] = fmaf(db, wv_dot(wb, xr), tb[r][c]);
         }
       }
     }
-    if (!active) continue;
-
-    // reduce across lanes (fixed butterfly) and write
+  };
+  // Reduce the row totals across the lanes (fixed butterfly) and write them.
+  auto finish = [&](int g) {
     float va[V], vb[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
@@ -198,6 +146,107 @@ qmv_cc_kernel(const CCParams p) {
         }
       }
     }
+  };
+  auto zero = [&]() {
+#pragma unroll
+    for (int r = 0; r < RW; ++r)
+#pragma unroll
+      for (int c = 0; c < NC; ++c) { ta[r][c] = 0.f; tb[r][c] = 0.f; }
+  };
+
+  // Rows of at most 64 blocks, one row group per warp (small matrices): the
+  // warp's blocks (at most two per lane and row) are loaded into registers
+  // before waiting for the previous kernel, which never writes weights, so
+  // after the wait only x is fetched. Same blocks, same order as the loop.
+  constexpr bool kPreload = !DUAL && RW * (QB / 4) * 2 <= 40;  // registers held across the wait
+  if (kPreload && nchunk == 1 && nb <= 64 && iters == 1) {
+    const int g = gfirst + warp;
+    const bool active = g < ngroups;
+    int rowidx[RW];
+#pragma unroll
+    for (int r = 0; r < RW; ++r) rowidx[r] = min(g * RW + r, p.rows - 1);
+    Blk<QT> q0[RW], q1[RW];
+    uint16_t s0[RW], s1[RW];
+    const int b0 = lane, b1 = lane + 32;
+    if (active) {
+#pragma unroll
+      for (int r = 0; r < RW; ++r) {
+        if (b0 < nb) {
+          q0[r].load(p.qa + (size_t)rowidx[r] * rowbytes + (size_t)b0 * QB);
+          s0[r] = ld_u16(p.sa + (size_t)rowidx[r] * nb + b0);
+        }
+        if (b1 < nb) {
+          q1[r].load(p.qa + (size_t)rowidx[r] * rowbytes + (size_t)b1 * QB);
+          s1[r] = ld_u16(p.sa + (size_t)rowidx[r] * nb + b1);
+        }
+      }
+    }
+    pdl_wait();
+    stage_x<QT, NC>(xs, xstride, p.x, k, cols, 0, nb);
+    __syncthreads();
+    if (!active) return;
+    zero();
+    if (b0 < nb) accumulate(q0, s0, q0, s0, b0);
+    if (b1 < nb) accumulate(q1, s1, q1, s1, b1);
+    finish(g);
+    return;
+  }
+
+  // The first 32 blocks of every row of this CTA's first row groups are pulled
+  // into L2 before waiting for the previous kernel (weights are never written
+  // by it), so the stream starts while that kernel drains and x is staged.
+  if (nchunk == 1 && iters > 0 && threadIdx.x < CC_WARPS * RW) {
+    const int row = gfirst * RW + (int)threadIdx.x;
+    if (row < p.rows) {
+      const int pb = (nb < 32 ? nb : 32) * QB;
+      l2_prefetch_bulk(p.qa + (size_t)row * rowbytes, (uint32_t)pb);
+      l2_prefetch_line(p.sa + (size_t)row * nb);
+      if (DUAL) {
+        l2_prefetch_bulk(p.qb + (size_t)row * rowbytes, (uint32_t)pb);
+        l2_prefetch_line(p.sb + (size_t)row * nb);
+      }
+    }
+  }
+  pdl_wait();
+
+  if (nchunk == 1) {
+    stage_x<QT, NC>(xs, xstride, p.x, k, cols, 0, nb);
+    __syncthreads();
+  }
+
+  for (int it = 0; it < iters; ++it) {
+    const int g = gfirst + warp + it * gstride;
+    const bool active = g < ngroups;
+    int rowidx[RW];
+#pragma unroll
+    for (int r = 0; r < RW; ++r) rowidx[r] = min(g * RW + r, p.rows - 1);
+    zero();
+    for (int ch = 0; ch < nchunk; ++ch) {
+      const int kb0 = ch * cb;
+      const int kb1 = min(nb, kb0 + cb);
+      if (nchunk > 1) {
+        __syncthreads();
+        stage_x<QT, NC>(xs, xstride, p.x, k, cols, kb0, kb1);
+        __syncthreads();
+      }
+      if (!active) continue;
+      for (int b = kb0 + lane; b < kb1; b += 32) {
+        Blk<QT> qa[RW], qb[RW];
+        uint16_t sa[RW], sb[RW];
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+          qa[r].load(p.qa + (size_t)rowidx[r] * rowbytes + (size_t)b * QB);
+          sa[r] = ld_u16(p.sa + (size_t)rowidx[r] * nb + b);
+          if (DUAL) {
+            qb[r].load(p.qb + (size_t)rowidx[r] * rowbytes + (size_t)b * QB);
+            sb[r] = ld_u16(p.sb + (size_t)rowidx[r] * nb + b);
+          }
+        }
+        accumulate(qa, sa, qb, sb, b - kb0);
+      }
+    }
+    if (!active) continue;
+    finish(g);
   }
 }
 
