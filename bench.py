@@ -424,8 +424,10 @@ def run_case(args):
 
 # The next steps around the step's calls, as single-kernel profiling targets
 # at their config sizes: greedy argmax and top-40 over one column of 248,320
-# logits; the MoE router (256 x 2048 f32, top-8) on one column.
-EXTRA_CASES = ("argmax", "topk40", "router")
+# logits; the MoE router (256 x 2048 f32, top-8) on one column; and the small
+# Q8_0 decode GEMV (2048 x 2048, one column, CUDA-core kernel), which the step
+# does not contain.
+EXTRA_CASES = ("argmax", "topk40", "router", "q8gemv2048")
 
 
 def run_extra_case(args, torch, qg):
@@ -441,6 +443,16 @@ def run_extra_case(args, torch, qg):
                 qg.qargmax_f32(x, idx[:, 0], val[:, 0], stream)
             else:
                 qg.qtopk_f32(x, k, idx, val, stream)
+    elif args.case == "q8gemv2048":
+        c = synth.small_q8_gemv()
+        blocks = torch.from_numpy(synth.to_gguf_blocks(c["qtype"], c["q"], c["scl"])).cuda()
+        q = torch.empty(c["q"].shape, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(c["scl"].shape, dtype=torch.int16, device="cuda")
+        qg.qrepack(c["qtype"], blocks, c["rows"], c["k"], q, sc)
+        x = torch.from_numpy(c["x"].view(np.int16)).cuda().view(torch.float16)
+        y = torch.empty((1, c["rows"]), dtype=torch.float32, device="cuda")
+        for _ in range(args.steps):
+            qg.qgemv_q8_0(q, sc, x, y, None, stream)
     else:
         w = torch.from_numpy((g.standard_normal((256, 2048)) * 0.02).astype(np.float32)).cuda()
         x = torch.from_numpy(synth.draw_x(g, 1, 2048).view(np.int16)).cuda().view(torch.float16)

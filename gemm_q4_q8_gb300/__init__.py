@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemm.so")
 
 EXPORTS = ("qg_status_str", "qgemv_q4_0", "qgemv_q8_0", "qgemm_cols", "qffn_gate_up_silu",
            "qmoe_workspace_bytes", "qmoe_experts", "qmoe_experts_noalloc", "qrepack",
-           "qargmax_f32", "qtopk_f32", "qmoe_router", "qg_kernel_launches")
+           "qargmax_f32", "qtopk_f32", "qmoe_router", "qg_kernel_launches", "qg_device_error")
 
 QG_MOE_NOALLOC_WS_BYTES = 8 << 20
 
@@ -71,6 +71,7 @@ def load(path: str | None = None):
     L.qmoe_router.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
     L.qg_kernel_launches.argtypes = []
     L.qg_kernel_launches.restype = C.c_uint64
+    L.qg_device_error.argtypes = [C.POINTER(C.c_int32)]
     for f in EXPORTS:
         if f not in ("qg_status_str", "qmoe_workspace_bytes", "qg_kernel_launches"):
             getattr(L, f).restype = i32
@@ -162,6 +163,18 @@ def qmoe_experts_noalloc(qtype, qg, sg, qu, su, qd, sd, n_expert, ffn, hidden, i
 def qg_kernel_launches() -> int:
     """Kernels launched by the library so far in this process."""
     return int(load().qg_kernel_launches())
+
+
+QG_DEV_ERR_WAIT = 1
+
+
+def qg_device_error() -> int:
+    """The current device's error word, then cleared (0: no error; bit
+    QG_DEV_ERR_WAIT: a tensor-core kernel gave up a wait, so some call since
+    the last read returned wrong outputs). Synchronises the device."""
+    v = C.c_int32(0)
+    _check("qg_device_error", load().qg_device_error(C.byref(v)))
+    return int(v.value)
 
 
 def qrepack(qtype, gguf, rows, k, q_out, scl_out, stream=None):

@@ -47,7 +47,7 @@ constexpr int TC_THREADS = (TC_CONSUMERS + 1) * 32;
 constexpr int TC_SMEM_BUDGET = 112 * 1024;  // two CTAs per SM
 constexpr long long TC_WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before giving up
 
-__device__ int32_t g_tc_error = 0;        // bit 1: a wait timed out
+__device__ int32_t g_tc_error = 0;        // QG_DEV_ERR_WAIT: a wait timed out
 
 // ------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -81,7 +81,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > TC_WAIT_LIMIT) {
-      atomicOr(&g_tc_error, 1);
+      atomicOr(&g_tc_error, QG_DEV_ERR_WAIT);
       return false;
     }
   }
@@ -685,3 +685,13 @@ cudaError_t tc_gemm(int qt, const void* q, const uint16_t* scl, const void* qu,
 }
 
 }  // namespace qg
+
+extern "C" qg_status qg_device_error(int32_t* bits_out) {
+  if (!bits_out) return QG_ERR_NULL;
+  int32_t v = 0;
+  const int32_t zero = 0;
+  if (cudaMemcpyFromSymbol(&v, qg::g_tc_error, sizeof(v)) != cudaSuccess) return QG_ERR_CUDA;
+  if (cudaMemcpyToSymbol(qg::g_tc_error, &zero, sizeof(zero)) != cudaSuccess) return QG_ERR_CUDA;
+  *bits_out = v;
+  return QG_OK;
+}

@@ -246,6 +246,20 @@ qg_status qtopk_f32(const float *x, int n, int ncols, int k, int32_t *idx_out,
  * ------------------------------------------------------------------------- */
 uint64_t qg_kernel_launches(void);
 
+/* ---------------------------------------------------------------------------
+ * Diagnostics: the current device's error word, read and then cleared.
+ * Not part of the method. Every wait of the tensor-core kernel (on its TMA
+ * data or on a free pipeline stage) is bounded (~2 s); a wait that gives up
+ * sets bit QG_DEV_ERR_WAIT and the kernel returns without its result, so the
+ * outputs of that call are wrong while the context stays usable. The word is
+ * shared by every call on the device since the last read.
+ *  - bits_out: host pointer, receives the word (0: no error).
+ *  - Synchronises the current device (a copy from a device symbol).
+ *  - QG_ERR_NULL if bits_out is null, QG_ERR_CUDA if the copies fail.
+ * ------------------------------------------------------------------------- */
+#define QG_DEV_ERR_WAIT 1
+qg_status qg_device_error(int32_t *bits_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -132,6 +132,17 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert gemv(lib) == 6
 
 
+def test_device_error_word(lib):
+    """qg_device_error: a null output is QG_ERR_NULL; without a GPU the read of
+    the device word fails loudly (QG_ERR_CUDA)."""
+    import ctypes as C
+    from conftest import gpu_available
+    assert lib.qg_device_error(None) == 1
+    if not gpu_available():
+        v = C.c_int32(-5)
+        assert lib.qg_device_error(C.byref(v)) == 6 and v.value == -5
+
+
 def test_sampling_argument_errors(lib):
     assert lib.qargmax_f32(ALIGNED, 0, 1, ALIGNED, None, None) == 2
     assert lib.qargmax_f32(ALIGNED, 10, 65, ALIGNED, None, None) == 2

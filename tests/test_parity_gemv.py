@@ -109,6 +109,17 @@ def test_q4_lm_head_shape_all_rows():
     assert_within(got, yr, gemv_bound(S), "Q4_0 248320x5120 C=1, every row")
 
 
+def test_no_device_error_after_tensor_core_calls():
+    """Every tensor-core wait is bounded; none gives up on ordinary calls, so the
+    device error word reads 0 afterwards (and reading clears it)."""
+    qg.qg_device_error()  # start from a clear word
+    for qtype, ncols in ((synth.Q4_0, 1), (synth.Q8_0, 8), (synth.Q4_0, 16)):
+        case = synth.gemv_case(qtype, 3000, 5120, ncols, residual=True, seed=50 + ncols)
+        check_case(case, api="cols", what=f"tensor-core {qtype} C={ncols}")
+    assert qg.qg_device_error() == 0
+    assert qg.qg_device_error() == 0
+
+
 def test_q4_large_one_column_sampled_rows():
     """One column of a large Q4_0 matrix (the tensor-core plan), ragged row tail."""
     case = synth.gemv_case(synth.Q4_0, 20000, 5120, 1, residual=True, seed=41)
