@@ -164,7 +164,10 @@ class GpuStep:
             self.m_err = t.zeros(1, dtype=t.int32, device="cuda")
             self.m_uniq = t.empty(m["ncols"] * m["topk"], dtype=t.int32, device="cuda")
 
-        # per-step inputs (device) and their pinned host copies (for e2e)
+        # Per-step inputs and outputs. Each direction is one flat buffer (every
+        # tensor a 256-byte aligned view into it), so a step moves its inputs
+        # up in one copy and its outputs down in one copy. Two device sets: the
+        # end-to-end loop copies one set while the kernels work on the other.
         self.host_in = {}
         if g is not None:
             self.host_in.update({"g_x": g["x"].view(np.int16), "g_y0": g["y0"]})
@@ -176,68 +179,118 @@ class GpuStep:
             self.host_in.update({"f_x": f["x"].view(np.int16), "f_y0": f["y0"]})
         if m is not None:
             self.host_in.update({"m_x": m["x"].view(np.int16), "m_ids": m["ids"], "m_rw": m["rw"]})
-        self.din = {k: d(v) for k, v in self.host_in.items()}
-        self.pin_in = {k: t.from_numpy(np.ascontiguousarray(v)).pin_memory()
-                       for k, v in self.host_in.items()}
-        f16 = t.float16
-        self.out = {}
+        tdt = {np.dtype(np.int16): t.int16, np.dtype(np.float32): t.float32,
+               np.dtype(np.int32): t.int32}
+        in_specs = [(k, v.shape, tdt[v.dtype]) for k, v in self.host_in.items()]
+        out_specs = []
         if g is not None:
-            self.out["g_y"] = t.empty((1, g["scl"].shape[0]), dtype=t.float32, device="cuda")
+            out_specs.append(("g_y", (1, g["scl"].shape[0]), t.float32))
         if l is not None:
-            self.out["l_y"] = t.empty((1, l["scl"].shape[0]), dtype=t.float32, device="cuda")
+            out_specs.append(("l_y", (1, l["scl"].shape[0]), t.float32))
         if tw is not None:
-            self.out["t_y"] = t.empty((8, tw["scl"].shape[0]), dtype=t.float32, device="cuda")
+            out_specs.append(("t_y", (8, tw["scl"].shape[0]), t.float32))
         if f is not None:
-            self.out["f_h"] = t.empty((16, 17408), dtype=f16, device="cuda")
-            self.out["f_y"] = t.empty((16, 5120), dtype=t.float32, device="cuda")
+            out_specs += [("f_h", (16, 17408), t.float16), ("f_y", (16, 5120), t.float32)]
         if m is not None:
-            self.out["m_y"] = t.empty((8, 2048), dtype=t.float32, device="cuda")
-        self.pin_out = {k: t.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.out.items()}
+            out_specs.append(("m_y", (8, 2048), t.float32))
 
-    def x16(self, key):
-        return self.din[key].view(self.torch.float16)
+        def layout(specs):
+            offs, off = {}, 0
+            for k, shape, dt in specs:
+                nbytes = int(np.prod(shape)) * t.empty((), dtype=dt).element_size()
+                offs[k] = (off, nbytes, shape, dt)
+                off = (off + nbytes + 255) // 256 * 256
+            return offs, max(off, 256)
 
-    def call(self, name: str, stream):
-        qg, o, m = self.qg, self.out, self.w.get("moe")
+        def views(flat, offs):
+            return {k: flat[o:o + n].view(dt).view(shape) for k, (o, n, shape, dt) in offs.items()}
+        in_offs, in_total = layout(in_specs)
+        out_offs, out_total = layout(out_specs)
+        self.pin_in_flat = t.zeros(in_total, dtype=t.uint8).pin_memory()
+        for k, v in views(self.pin_in_flat, in_offs).items():
+            v.copy_(t.from_numpy(np.ascontiguousarray(self.host_in[k])))
+        self.pin_out_flat = t.zeros(out_total, dtype=t.uint8).pin_memory()
+        self.pin_out = views(self.pin_out_flat, out_offs)
+        self.din_flat = [self.pin_in_flat.cuda() for _ in range(2)]
+        self.dout_flat = [t.zeros(out_total, dtype=t.uint8, device="cuda") for _ in range(2)]
+        self.din_sets = [views(fl, in_offs) for fl in self.din_flat]
+        self.out_sets = [views(fl, out_offs) for fl in self.dout_flat]
+        self.din, self.out = self.din_sets[0], self.out_sets[0]
+        self.copy_stream = None
+
+    def call(self, name: str, stream, buf: int = 0):
+        qg, m = self.qg, self.w.get("moe")
+        din, o = self.din_sets[buf], self.out_sets[buf]
+
+        def x16(key):
+            return din[key].view(self.torch.float16)
         if name == "gemv":
-            qg.qgemv_q4_0(self.g_q, self.g_s, self.x16("g_x"), o["g_y"], self.din["g_y0"], stream)
+            qg.qgemv_q4_0(self.g_q, self.g_s, x16("g_x"), o["g_y"], din["g_y0"], stream)
         elif name == "lmhead":
-            qg.qgemv_q8_0(self.l_q, self.l_s, self.x16("l_x"), o["l_y"], None, stream)
+            qg.qgemv_q8_0(self.l_q, self.l_s, x16("l_x"), o["l_y"], None, stream)
         elif name == "twins":
-            qg.qgemv_q4_0(self.t_q, self.t_s, self.x16("t_x"), o["t_y"], None, stream)
+            qg.qgemv_q4_0(self.t_q, self.t_s, x16("t_x"), o["t_y"], None, stream)
         elif name == "gateup":
             qg.qffn_gate_up_silu(qg.Q4_0, self.f_qg, self.f_sg, self.f_qu, self.f_su,
-                                 self.x16("f_x"), o["f_h"], stream)
+                                 x16("f_x"), o["f_h"], stream)
         elif name == "down":
-            qg.qgemm_cols(qg.Q4_0, self.f_qd, self.f_sd, o["f_h"], o["f_y"], self.din["f_y0"], stream)
+            qg.qgemm_cols(qg.Q4_0, self.f_qd, self.f_sd, o["f_h"], o["f_y"], din["f_y0"], stream)
         elif name == "moe":
             mm = self.m
             qg.qmoe_experts(qg.Q8_0, mm["qg"], mm["sg"], mm["qu"], mm["su"], mm["qd"], mm["sd"],
-                            m["n_expert"], m["ffn"], m["hidden"], self.din["m_ids"],
-                            self.din["m_rw"], self.x16("m_x"), o["m_y"], self.m_ws, y0=None,
+                            m["n_expert"], m["ffn"], m["hidden"], din["m_ids"],
+                            din["m_rw"], x16("m_x"), o["m_y"], self.m_ws, y0=None,
                             shared=self.m_sh, err_flag=self.m_err, uniq_ids_out=self.m_uniq,
                             stream=stream)
 
-    def step(self, stream, events=None):
+    def step(self, stream, events=None, buf: int = 0):
         for i, name in enumerate(KERNELS):
             if events is not None:
                 events[i].record(stream)
-            self.call(name, stream)
+            self.call(name, stream, buf)
         if events is not None:
             events[len(KERNELS)].record(stream)
 
-    def step_e2e(self, stream):
-        """Inputs copied from pinned host memory, outputs copied back."""
-        for k, v in self.pin_in.items():
-            self.din[k].copy_(v, non_blocking=True)
-        self.step(stream)
-        for k, v in self.out.items():
-            self.pin_out[k].copy_(v, non_blocking=True)
+    def step_e2e(self, stream, i: int):
+        """Step i end to end: its inputs go up from pinned host memory, the six
+        calls run, its outputs come down to pinned host memory. Copies run on a
+        copy stream with device buffer set i % 2, so step i+1's upload and step
+        i's download overlap the kernels of the neighbouring step; events keep
+        every buffer's writes and reads in order."""
+        t = self.torch
+        if self.copy_stream is None:
+            self.copy_stream = t.cuda.Stream()
+            self.ev = {k: [t.cuda.Event(), t.cuda.Event()] for k in ("up", "run", "down")}
+            self.used = [False, False]
+        cs, b = self.copy_stream, i % 2
+        ev = self.ev
+        with t.cuda.stream(cs):
+            if i == 0:
+                cs.wait_stream(stream)           # the timed region starts before the first upload
+            if self.used[b]:
+                cs.wait_event(ev["run"][b])      # step i-2 has finished reading set b
+            self.din_flat[b].copy_(self.pin_in_flat, non_blocking=True)
+            ev["up"][b].record(cs)
+        stream.wait_event(ev["up"][b])
+        if self.used[b]:
+            stream.wait_event(ev["down"][b])     # step i-2's outputs have left set b
+        self.step(stream, buf=b)
+        ev["run"][b].record(stream)
+        with t.cuda.stream(cs):
+            cs.wait_event(ev["run"][b])
+            self.pin_out_flat.copy_(self.dout_flat[b], non_blocking=True)
+            ev["down"][b].record(cs)
+        self.used[b] = True
+
+    def e2e_join(self, stream):
+        """Make `stream` wait for every copy issued so far."""
+        if self.copy_stream is not None:
+            stream.wait_stream(self.copy_stream)
 
     def e2e_bytes(self):
-        bi = sum(v.numel() * v.element_size() for v in self.pin_in.values())
-        bo = sum(v.numel() * v.element_size() for v in self.pin_out.values())
-        return bi, bo
+        """Bytes of the one upload and the one download of a step (the flat
+        buffers: the tensors plus their alignment padding)."""
+        return self.pin_in_flat.numel(), self.pin_out_flat.numel()
 
 
 # -------------------------------------------------------------- clocks
@@ -835,20 +888,25 @@ def main(argv=None):
 
     # ---- end to end through the public API from pinned host buffers
     e2e_steps = max(3, min(args.steps, 100))
-    for _ in range(2):
-        gs.step_e2e(stream)
+    for i in range(2):
+        gs.step_e2e(stream, i)
+    gs.e2e_join(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for _ in range(e2e_steps):
-        gs.step_e2e(stream)
+    for i in range(e2e_steps):
+        gs.step_e2e(stream, i)
+    gs.e2e_join(stream)   # the last step's outputs are on the host before f1
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, torch, device) / e2e_steps
     bi, bo = gs.e2e_bytes()
+    # the outputs that reached the host equal the device-resident step's, bit for bit
+    # (same inputs, deterministic kernels)
+    e2e_match = all(torch.equal(gs.pin_out[k], v.cpu()) for k, v in gs.out_sets[0].items())
 
     peak, peak_kind = peaks()
     lm_ms = per_kernel_ms["lmhead"]
@@ -887,11 +945,14 @@ def main(argv=None):
         "breakdown": breakdown,
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms, "outputs_match_device_step": bool(e2e_match)},
         "gpu_launches": int(launches),
         "timing": "value: one CUDA graph per step (all calls), replayed back to back; "
                   "breakdown: one graph per call, replayed back to back with a CUDA event "
-                  "between consecutive graphs (includes each graph's launch gap)",
+                  "between consecutive graphs (includes each graph's launch gap); e2e: eager "
+                  "calls, every step's inputs uploaded from and outputs downloaded to pinned "
+                  "host memory on a copy stream (two device buffer sets, so one step's copies "
+                  "overlap the neighbouring step's kernels), all inside the timed region",
         "clocks": clk.summary(t_wall0, t_wall1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
