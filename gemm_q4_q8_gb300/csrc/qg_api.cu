@@ -4,8 +4,11 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <unordered_map>
+#include <utility>
 
 #include "qg_internal.h"
 #include "qgemm.h"
@@ -24,6 +27,55 @@ int device_sm_count() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+// Kernel preparation, cached per device. The dynamic shared-memory limit of a
+// kernel is only ever raised (to the largest size any call has needed), so a
+// launch on one host thread never finds the limit lowered by another thread
+// between its check and its launch.
+namespace {
+std::mutex g_kmu;
+std::map<std::pair<int, const void*>, size_t> g_smem_limit;          // (device, kernel)
+std::map<std::tuple<int, const void*, int, size_t>, int> g_occupancy;  // (device, kernel, threads, smem)
+}  // namespace
+
+cudaError_t prepare_kernel(const void* kern, size_t smem, bool nonportable_cluster) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_kmu);
+  auto it = g_smem_limit.find({dev, kern});
+  if (it == g_smem_limit.end()) {
+    if (nonportable_cluster &&
+        (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+      return e;
+    it = g_smem_limit.emplace(std::make_pair(dev, kern), (size_t)0).first;
+  }
+  if (smem > it->second) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+      return e;
+    it->second = smem;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t kernel_occupancy(const void* kern, int threads, size_t smem, int* occ) {
+  cudaError_t e = prepare_kernel(kern, smem, false);
+  if (e != cudaSuccess) return e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_kmu);
+  const auto key = std::make_tuple(dev, kern, threads, smem);
+  auto it = g_occupancy.find(key);
+  if (it == g_occupancy.end()) {
+    int n = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem)) != cudaSuccess)
+      return e;
+    it = g_occupancy.emplace(key, n < 1 ? 1 : n).first;
+  }
+  *occ = it->second;
+  return cudaSuccess;
 }
 
 static std::atomic<uint64_t> g_launches{0};

@@ -263,16 +263,9 @@ static cudaError_t launch_cc_t(const CCParams& p0, cudaStream_t s, int* nlaunch)
   p.cb = cb;
   const size_t smem = (size_t)NC * cb * QK * sizeof(float);
   auto kern = qmv_cc_kernel<QT, NC, RW, DUAL, EPI>;
-  static int occ = -1;
-  static size_t occ_smem = 0;
-  if (occ < 0 || occ_smem != smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, CC_THREADS, smem);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) occ = 1;
-    occ_smem = smem;
-  }
+  int occ = 1;
+  cudaError_t e = kernel_occupancy(reinterpret_cast<const void*>(kern), CC_THREADS, smem, &occ);
+  if (e != cudaSuccess) return e;
   const long ngroups = (p.rows + RW - 1) / RW;
   long grid = (ngroups + CC_WARPS - 1) / CC_WARPS;
   const long maxgrid = (long)device_sm_count() * occ;

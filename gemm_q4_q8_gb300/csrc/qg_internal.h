@@ -15,6 +15,15 @@ namespace qg {
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Raise `kern`'s dynamic shared-memory limit on the current device to at least
+// `smem` (never lowers it), and allow cluster sizes above 8 when asked; cached
+// per device, safe from several host threads.
+cudaError_t prepare_kernel(const void* kern, size_t smem, bool nonportable_cluster);
+
+// prepare_kernel, then how many CTAs of `threads` threads and `smem` bytes of
+// dynamic shared memory stay resident per SM (at least 1); cached per device.
+cudaError_t kernel_occupancy(const void* kern, int threads, size_t smem, int* occ);
+
 // Count one kernel launch (see qg_kernel_launches).
 void note_launch(int n = 1);
 

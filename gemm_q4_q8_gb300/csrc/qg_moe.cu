@@ -342,12 +342,9 @@ bool moe_shape_supported(int ffn, int hidden, int ncols, int topk) {
 template <class K>
 static cudaError_t launch_moe(K kern, int threads, long grid_max_units, int multiple, size_t smem,
                               const MoeDev& d, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   int occ = 1;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+  cudaError_t e = kernel_occupancy(reinterpret_cast<const void*>(kern), threads, smem, &occ);
   if (e != cudaSuccess) return e;
-  if (occ < 1) occ = 1;
   long grid = (long)device_sm_count() * occ;
   if (grid > grid_max_units) grid = grid_max_units;
   grid = grid / multiple * multiple;

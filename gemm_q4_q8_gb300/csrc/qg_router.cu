@@ -224,9 +224,7 @@ static cudaError_t router_go(size_t smem, const float* w, const __half* x, int E
                              int ncols, int topk, float* logits, int32_t* ids, float* rw,
                              cudaStream_t s) {
   auto kern = router_kernel<NC, XS, VEC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), smem, true);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(RT_CLUSTER), dim3(RT_THREADS), smem, s, RT_CLUSTER, LC_L1, w, x, E,
                     hidden, ncols, topk, logits, ids, rw);

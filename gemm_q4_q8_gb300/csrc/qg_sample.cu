@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(SMP_THREADS) topk_kernel(const float* __restri
 // ----------------------------------------------------------------- launch
 cudaError_t argmax_launch(const float* x, int n, int ncols, int32_t* idx, float* val,
                           cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(argmax_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(argmax_kernel), 0, true);
   if (e != cudaSuccess) return e;
   return launch_pdl(argmax_kernel, dim3((unsigned)(ncols * AMX_CLUSTER)), dim3(SMP_THREADS), 0, s,
                     AMX_CLUSTER, LC_L1, x, n, idx, val);
@@ -515,9 +515,7 @@ cudaError_t topk_launch(const float* x, int n, int ncols, int k, int32_t* idx, f
   while (kp < k) kp <<= 1;
   const size_t smem = stage_bytes + ((size_t)TK_CAND + (size_t)TK_CLUSTER * kp) * sizeof(uint64_t);
   auto kern = v4 ? topk_kernel<true> : topk_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), smem, true);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3((unsigned)(ncols * TK_CLUSTER)), dim3(SMP_THREADS), smem, s,
                     TK_CLUSTER, LC_L1, x, n, k, idx, val, staged, (int)stage_bytes);

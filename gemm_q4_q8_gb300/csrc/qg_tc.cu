@@ -636,7 +636,7 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
   p.y = y;
   p.h = reinterpret_cast<__half*>(h);
   auto kern = tc_kernel<QT, NT, DUAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), cfg.smem, false);
   if (e != cudaSuccess) return e;
   const int ntile = (rows + TC_BM - 1) / TC_BM;
   (void)S::NF;
@@ -649,8 +649,8 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
 // Shapes the tensor-core plan takes: K a multiple of 256, any column count
 // from 1 to 16, except that matrices of at most 2^22 weights with K <= 3072
 // keep 1-8 columns on the CUDA cores (their fixed latency is lower there:
-// 2048 x 2048 Q8_0 takes 4.1 us on CUDA cores and 6.8 us here at 1 column,
-// 7.5 and 6.8 us at 8). For 1-8 columns the choice depends on the matrix only,
+// 2048 x 2048 Q8_0 takes 2.7 us on CUDA cores and 6.8 us here at 1 column,
+// 7.3 and 6.8 us at 8). For 1-8 columns the choice depends on the matrix only,
 // and the plan is the same (one n-tile of 8), so the 1-column GEMV and its
 // 2-8-column twins give bit-identical columns: the mma computes each output
 // column from that column alone, and the CUDA-core twins repeat the 1-column
