@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(_HERE, "libqgemm.so")
 
 EXPORTS = ("qg_status_str", "qgemv_q4_0", "qgemv_q8_0", "qgemm_cols", "qffn_gate_up_silu",
            "qmoe_workspace_bytes", "qmoe_experts", "qmoe_experts_noalloc", "qrepack",
-           "qargmax_f32", "qtopk_f32", "qmoe_router", "qg_kernel_launches", "qg_device_error")
+           "qargmax_f32", "qtopk_f32", "qmoe_router", "qg_kernel_launches", "qg_device_error",
+           "qg_last_cuda_error", "qg_last_cuda_error_string")
 
 QG_MOE_NOALLOC_WS_BYTES = 8 << 20
 
@@ -72,8 +73,12 @@ def load(path: str | None = None):
     L.qg_kernel_launches.argtypes = []
     L.qg_kernel_launches.restype = C.c_uint64
     L.qg_device_error.argtypes = [C.POINTER(C.c_int32)]
+    L.qg_last_cuda_error.argtypes = []
+    L.qg_last_cuda_error_string.argtypes = []
+    L.qg_last_cuda_error_string.restype = C.c_char_p
     for f in EXPORTS:
-        if f not in ("qg_status_str", "qmoe_workspace_bytes", "qg_kernel_launches"):
+        if f not in ("qg_status_str", "qmoe_workspace_bytes", "qg_kernel_launches",
+                     "qg_last_cuda_error_string"):
             getattr(L, f).restype = i32
     _lib = L
     return L
@@ -81,7 +86,10 @@ def load(path: str | None = None):
 
 def _check(fn: str, st: int):
     if st != 0:
-        raise QGError(fn, st, load().qg_status_str(st).decode())
+        msg = load().qg_status_str(st).decode()
+        if st == 6:  # QG_ERR_CUDA: name the CUDA error behind it
+            msg += ": " + load().qg_last_cuda_error_string().decode()
+        raise QGError(fn, st, msg)
 
 
 def _ptr(t):

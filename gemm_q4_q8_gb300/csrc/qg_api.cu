@@ -2,6 +2,7 @@
 // dispatch to the kernels on the caller's stream. Nothing here allocates.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 
 #include <atomic>
 #include <map>
@@ -78,6 +79,11 @@ cudaError_t kernel_occupancy(const void* kern, int threads, size_t smem, int* oc
   return cudaSuccess;
 }
 
+// The CUDA error behind the latest QG_ERR_CUDA returned on this host thread.
+static thread_local cudaError_t t_last_cuda = cudaSuccess;
+void note_cuda_error(cudaError_t e) { t_last_cuda = e; }
+cudaError_t last_cuda_error() { return t_last_cuda; }
+
 static std::atomic<uint64_t> g_launches{0};
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
@@ -110,7 +116,11 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return pa < pb + nb && pb < pa + na;
 }
 
-qg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QG_OK : QG_ERR_CUDA; }
+qg_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return QG_OK;
+  qg::note_cuda_error(e);
+  return QG_ERR_CUDA;
+}
 
 // Common checks of a (rows x k) matrix product with ncols input columns.
 qg_status check_matmul(int t, const void* q, const uint16_t* scl, int rows, int k,
@@ -131,7 +141,21 @@ qg_status check_matmul(int t, const void* q, const uint16_t* scl, int rows, int 
 }
 
 // Device readiness (a device must be present and current).
-qg_status check_device() { return qg::device_sm_count() > 0 ? QG_OK : QG_ERR_CUDA; }
+qg_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  // A host thread's first runtime calls need not bind the device's primary
+  // context, and the tensor-core path calls the driver (tensor-map encoding)
+  // before its first launch: on a fresh thread that failed with invalid value.
+  // Make the context current once per thread and device.
+  static thread_local int bound = -1;
+  if (bound != dev) {
+    if ((e = cudaSetDevice(dev)) != cudaSuccess) return from_cuda(e);
+    bound = dev;
+  }
+  return qg::device_sm_count() > 0 ? QG_OK : from_cuda(cudaErrorNoDevice);
+}
 
 qg_status gemv_any(int t, const void* q, const uint16_t* scl, int rows, int k,
                    const uint16_t* x, int ncols, const float* y0, float* y, cudaStream_t s,
@@ -146,7 +170,7 @@ qg_status gemv_any(int t, const void* q, const uint16_t* scl, int rows, int k,
     const int nc = ncols - c0 < 8 ? ncols - c0 : 8;
     cudaError_t e = qg::cc_gemv(t, q, scl, rows, k, x + (size_t)c0 * k, nc,
                                 y0 ? y0 + (size_t)c0 * rows : nullptr, y + (size_t)c0 * rows, s);
-    if (e != cudaSuccess) return QG_ERR_CUDA;
+    if (e != cudaSuccess) return from_cuda(e);
   }
   return QG_OK;
 }
@@ -154,6 +178,15 @@ qg_status gemv_any(int t, const void* q, const uint16_t* scl, int rows, int k,
 }  // namespace
 
 extern "C" {
+
+int qg_last_cuda_error(void) { return (int)qg::last_cuda_error(); }
+
+const char* qg_last_cuda_error_string(void) {
+  static thread_local char buf[256];
+  const cudaError_t e = qg::last_cuda_error();
+  snprintf(buf, sizeof(buf), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return buf;
+}
 
 const char* qg_status_str(qg_status s) {
   switch (s) {
@@ -201,7 +234,7 @@ qg_status qffn_gate_up_silu(qg_type t, const void* qg, const uint16_t* sg, const
     const int nc = ncols - c0 < 8 ? ncols - c0 : 8;
     cudaError_t e = qg::cc_gate_up_silu((int)t, qg, sg, qu, su, rows, k, x + (size_t)c0 * k, nc,
                                         h + (size_t)c0 * rows, stream);
-    if (e != cudaSuccess) return QG_ERR_CUDA;
+    if (e != cudaSuccess) return from_cuda(e);
   }
   return QG_OK;
 }

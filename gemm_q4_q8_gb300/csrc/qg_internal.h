@@ -24,6 +24,11 @@ cudaError_t prepare_kernel(const void* kern, size_t smem, bool nonportable_clust
 // dynamic shared memory stay resident per SM (at least 1); cached per device.
 cudaError_t kernel_occupancy(const void* kern, int threads, size_t smem, int* occ);
 
+// Remember the CUDA error behind a QG_ERR_CUDA on this host thread
+// (qg_last_cuda_error), and read it back.
+void note_cuda_error(cudaError_t e);
+cudaError_t last_cuda_error();
+
 // Count one kernel launch (see qg_kernel_launches).
 void note_launch(int n = 1);
 

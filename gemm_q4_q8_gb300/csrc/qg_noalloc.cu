@@ -41,12 +41,19 @@ void* g_ws_addr[kMaxDevices] = {nullptr};
 // Device address of the array on the current device (set up on first use).
 qg_status ws_address(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QG_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    qg::note_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+    return QG_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_ws_addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_moe_noalloc_ws) != cudaSuccess || p == nullptr)
+    e = cudaGetSymbolAddress(&p, g_moe_noalloc_ws);
+    if (e != cudaSuccess || p == nullptr) {
+      qg::note_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
       return QG_ERR_CUDA;
+    }
     g_ws_addr[dev] = p;
   }
   *out = g_ws_addr[dev];

@@ -260,6 +260,16 @@ uint64_t qg_kernel_launches(void);
 #define QG_DEV_ERR_WAIT 1
 qg_status qg_device_error(int32_t *bits_out);
 
+/* ---------------------------------------------------------------------------
+ * Diagnostics: the CUDA runtime error behind the latest QG_ERR_CUDA that a
+ * call of this library returned on the calling host thread (a cudaError_t
+ * value; 0 if there was none), and its name and description. The string
+ * belongs to the library and stays valid until the thread's next call of
+ * qg_last_cuda_error_string. Not part of the method.
+ * ------------------------------------------------------------------------- */
+int qg_last_cuda_error(void);
+const char *qg_last_cuda_error_string(void);
+
 #ifdef __cplusplus
 }
 #endif

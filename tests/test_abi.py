@@ -128,8 +128,11 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     from conftest import gpu_available
     if gpu_available():
         pytest.skip("a GPU is present")
-    # valid arguments: the library must fail loudly (no CPU fallback)
+    # valid arguments: the library must fail loudly (no CPU fallback), and it
+    # names the CUDA error behind QG_ERR_CUDA on this thread
     assert gemv(lib) == 6
+    assert lib.qg_last_cuda_error() != 0
+    assert lib.qg_last_cuda_error_string().decode().startswith("cudaError")
 
 
 def test_device_error_word(lib):
