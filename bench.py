@@ -98,6 +98,23 @@ def make_workload(seed: int = 0, only=None) -> dict:
     return w
 
 
+def activation_bytes() -> dict:
+    """Algorithmic bytes of a step's activations, residuals and outputs per
+    call (what each kernel must read or write besides weights): x f16 read,
+    y0 f32 read, y f32 or h f16 written; the FFN's h is written by gate/up and
+    read by down; the MoE reads x, the ids and routing weights, writes y and
+    writes then reads its h (f16 [cols][top-k + 1][ffn])."""
+    f16, f32, i32 = 2, 4, 4
+    return {
+        "gemv": 5120 * f16 + 5120 * f32 + 5120 * f32,
+        "lmhead": 5120 * f16 + 248320 * f32,
+        "twins": 8 * 5120 * f16 + 8 * 17408 * f32,
+        "gateup": 16 * 5120 * f16 + 16 * 17408 * f16,
+        "down": 16 * 17408 * f16 + 16 * 5120 * f32 + 16 * 5120 * f32,
+        "moe": 8 * 2048 * f16 + 8 * 8 * (i32 + f32) + 8 * 2048 * f32 + 2 * 8 * 9 * 512 * f16,
+    }
+
+
 def weight_bytes(w: dict, uniq_count: int) -> dict:
     wb = {}
     wb["gemv"] = synth.weight_bytes(synth.Q4_0, 5120, 5120)
@@ -932,7 +949,9 @@ def main(argv=None):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "weights": "Q4_0/Q8_0 blocks, f16 scales",
                    "activations": "f16", "accumulate": "f32",
-                   "step_weight_bytes": step_bytes, "moe_unique_experts": uniq,
+                   "step_weight_bytes": step_bytes,
+                   "step_total_bytes": step_bytes + sum(activation_bytes().values()),
+                   "moe_unique_experts": uniq,
                    "l2": "inputs larger than L2: each step streams ~1.8 GB of distinct weights "
                          "(L2 is 129 MB), so no step finds the previous step's weights in L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
