@@ -30,7 +30,13 @@
  *    and the call returns without synchronising.
  *  - Argument errors (NULL, shape, alignment, type, workspace) are detected on
  *    the host before anything is launched and returned synchronously; nothing
- *    is written. A launch failure returns QG_ERR_CUDA.
+ *    is written. A launch failure returns QG_ERR_CUDA, and qg_last_cuda_error
+ *    on the same host thread names the CUDA error behind it.
+ *  - Host threads: calls may come from several threads at once (each on its
+ *    own stream, or ordered by the caller). Per-device kernel set-up happens
+ *    once, under a lock. A thread's first call makes the current device's
+ *    primary context current on that thread (cudaSetDevice); make that first
+ *    call outside any stream capture.
  *  - Alignment: quant and scale arrays and X must be 16-byte aligned; Y, y0
  *    4-byte aligned; H 2-byte aligned.
  *  - Residual: y0 may be NULL (no residual) or point to f32 [ncols][rows];
