@@ -47,6 +47,8 @@ def lib():
         L.qref_f16_to_f64.restype = C.c_double
         L.qref_silu.argtypes = [C.c_double]
         L.qref_silu.restype = C.c_double
+        L.qref_silu_prime.argtypes = [C.c_double]
+        L.qref_silu_prime.restype = C.c_double
         L.qref_h_bound.argtypes = [C.c_double] * 4
         L.qref_h_bound.restype = C.c_double
         L.qref_dequant_row.argtypes = [i32, vp, vp, i32, dp]
@@ -85,6 +87,10 @@ def f16_to_f64(bits: int) -> float:
 
 def silu(z: float) -> float:
     return lib().qref_silu(float(z))
+
+
+def silu_prime(z: float) -> float:
+    return lib().qref_silu_prime(float(z))
 
 
 def h_bound(g, u, Sg, Su):

@@ -220,17 +220,50 @@ int qref_ffn_gate_up_silu(int type, const void *qg, const uint16_t *sg, const vo
 
 /* ---------------------------------------------------------------- MoE */
 
+/* SiLU'(z) = sigma(z) (1 + z (1 - sigma(z))), sigma(z) = 1 / (1 + e^-z): the
+ * product rule applied to z * sigma(z), with sigma' = sigma (1 - sigma). */
+double qref_silu_prime(double z) {
+  double s = 1.0 / (1.0 + exp(-z));
+  return s * (1.0 + z * (1.0 - s));
+}
+
+/* The one critical point of SiLU: SiLU'(z) = sigma(z) f(z) with
+ * f(z) = 1 + z (1 - sigma(z)); f > 0 for z >= 0, and on z < 0 f is increasing
+ * (f' = (1 - sigma)(1 - z sigma) > 0) from -inf to 1, so it has exactly one
+ * root, between -2 and -1 (f(-2) < 0 < f(-1)). Found by bisection. */
+static double silu_critical_point(void) {
+  double a = -2.0, b = -1.0;
+  for (int i = 0; i < 200 && b - a > 0.0; ++i) {
+    double m = 0.5 * (a + b);
+    if (m == a || m == b) break;
+    if (qref_silu_prime(m) < 0.0) a = m; else b = m;
+  }
+  return 0.5 * (a + b);
+}
+
 /* Bound on |h_gpu - h| for one element of a gated FFN whose projections each
- * carry the GEMV tolerance e = 1e-3 * S + 1e-6, followed by SiLU * up in f32
- * and one rounding to f16:
- *   |SiLU(g') u' - SiLU(g) u| <= 1.1 |eg| (|u| + eu) + |SiLU(g)| eu
- * (|SiLU'| <= 1.1 everywhere), plus 2^-11 of the result and 2^-24 absolute
- * for the f16 rounding, plus 1e-6 relative for the f32 evaluation. */
+ * carry the GEMV tolerance e = 1e-3 * S + 1e-6 (g' = g + dg, |dg| <= eg; the
+ * same for u), followed by SiLU * up in f32 and one rounding to f16.
+ * SiLU is monotone on each side of its critical point z0, so over the interval
+ * [g - eg, g + eg] its extremes lie at the two ends or at z0 (if inside), and
+ *   D = max |SiLU(g') - SiLU(g)| = max(|SiLU(g + eg) - SiLU(g)|,
+ *                                      |SiLU(g - eg) - SiLU(g)|,
+ *                                      |SiLU(z0) - SiLU(g)| if z0 is inside)
+ * exactly. With |u'| <= |u| + eu:
+ *   |SiLU(g') u' - SiLU(g) u| <= D (|u| + eu) + |SiLU(g)| eu,
+ * which to first order is 1e-3 (|SiLU'(g)| |u| Sg + |SiLU(g)| Su). Added: one
+ * f16 rounding of the result (2^-11 relative, 2^-24 absolute for subnormals)
+ * and 1e-6 relative for the f32 evaluation of SiLU(g) * u. */
 double qref_h_bound(double g, double u, double Sg, double Su) {
+  static double z0 = 0.0;
+  if (z0 == 0.0) z0 = silu_critical_point();
   double eg = 1e-3 * Sg + 1e-6, eu = 1e-3 * Su + 1e-6;
-  double h = qref_silu(g) * u;
-  double prop = 1.1 * eg * (fabs(u) + eu) + fabs(qref_silu(g)) * eu;
-  return prop + ldexp(fabs(h) + prop, -11) + ldexp(1.0, -24) + 1e-6 * fabs(h);
+  double sg = qref_silu(g);
+  double h = sg * u;
+  double D = fmax(fabs(qref_silu(g + eg) - sg), fabs(qref_silu(g - eg) - sg));
+  if (g - eg <= z0 && z0 <= g + eg) D = fmax(D, fabs(qref_silu(z0) - sg));
+  double prop = D * (fabs(u) + eu) + fabs(sg) * eu;
+  return prop + ldexp(fabs(h) + prop, -11) + ldexp(1.0, -24) + 1e-6 * (fabs(h) + prop);
 }
 
 typedef struct {
