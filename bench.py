@@ -960,7 +960,8 @@ def main(argv=None):
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": lmhead_traffic(w["lmhead"]["rows"]),
                      "traffic_note": "dram read+write bytes per launch, ncu capture of a "
-                                     "65,536-row cut scaled by rows (profiles/lmhead_q8_gemv.md)"},
+                                     "65,536-row cut scaled by rows (committed LM-head "
+                                     "capture summary under profiles/)"},
         "breakdown": breakdown,
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,

@@ -23,10 +23,15 @@ EXPORTS = ("qg_status_str", "qgemv_q4_0", "qgemv_q8_0", "qgemm_cols", "qffn_gate
            "qargmax_f32", "qtopk_f32", "qmoe_router", "qg_kernel_launches", "qg_device_error",
            "qg_last_cuda_error", "qg_last_cuda_error_string")
 
-QG_MOE_NOALLOC_WS_BYTES = 8 << 20
+QG_MOE_NOALLOC_WS_BYTES = 1 << 20
 
-STATUS = {0: "QG_OK", 1: "QG_ERR_NULL", 2: "QG_ERR_SHAPE", 3: "QG_ERR_ALIGN", 4: "QG_ERR_TYPE",
-          5: "QG_ERR_WORKSPACE", 6: "QG_ERR_CUDA", 7: "QG_ERR_ALIAS"}
+# qg_status values (include/qgemm.h)
+QG_OK, QG_ERR_NULL, QG_ERR_SHAPE, QG_ERR_ALIGN, QG_ERR_TYPE = 0, 1, 2, 3, 4
+QG_ERR_WORKSPACE, QG_ERR_CUDA, QG_ERR_ALIAS = 5, 6, 7
+STATUS = {QG_OK: "QG_OK", QG_ERR_NULL: "QG_ERR_NULL", QG_ERR_SHAPE: "QG_ERR_SHAPE",
+          QG_ERR_ALIGN: "QG_ERR_ALIGN", QG_ERR_TYPE: "QG_ERR_TYPE",
+          QG_ERR_WORKSPACE: "QG_ERR_WORKSPACE", QG_ERR_CUDA: "QG_ERR_CUDA",
+          QG_ERR_ALIAS: "QG_ERR_ALIAS"}
 
 
 class QGError(RuntimeError):
@@ -87,7 +92,7 @@ def load(path: str | None = None):
 def _check(fn: str, st: int):
     if st != 0:
         msg = load().qg_status_str(st).decode()
-        if st == 6:  # QG_ERR_CUDA: name the CUDA error behind it
+        if st == QG_ERR_CUDA:  # name the CUDA error behind it
             msg += ": " + load().qg_last_cuda_error_string().decode()
         raise QGError(fn, st, msg)
 
@@ -155,8 +160,10 @@ def qmoe_experts(qtype, qg, sg, qu, su, qd, sd, n_expert, ffn, hidden, ids, rw, 
 
 def qmoe_experts_noalloc(qtype, qg, sg, qu, su, qd, sd, n_expert, ffn, hidden, ids, rw, x, y,
                          y0=None, shared=None, err_flag=None, uniq_ids_out=None, stream=None):
-    """qmoe_experts with the library's built-in workspace (no caller allocation);
-    problems needing more than QG_MOE_NOALLOC_WS_BYTES raise QG_ERR_WORKSPACE."""
+    """qmoe_experts with the library's built-in workspace of QG_MOE_NOALLOC_WS_BYTES
+    (no caller allocation): for callers that cannot allocate device memory. Every
+    shape qmoe_experts accepts fits; calls that overlap on the GPU race on the
+    shared workspace."""
     sh = None
     if shared is not None:
         sh = C.pointer(QGExpert(*[_ptr(shared[n]) for n in ("qg", "sg", "qu", "su", "qd", "sd")]))

@@ -87,6 +87,15 @@ cudaError_t last_cuda_error() { return t_last_cuda; }
 static std::atomic<uint64_t> g_launches{0};
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+qg_status moe_check_shape(int t, int n_expert, int ffn, int hidden, int ncols, int topk) {
+  if (t != QG_Q4_0 && t != QG_Q8_0) return QG_ERR_TYPE;
+  if (n_expert < 1 || n_expert > QG_MOE_MAX_EXPERTS || ffn <= 0 || hidden <= 0 || (ffn % 32) ||
+      (hidden % 32) || ncols < 1 || ncols > 16 || topk < 1 || topk > 16 ||
+      !moe_shape_supported(ffn, hidden, ncols, topk))
+    return QG_ERR_SHAPE;
+  return QG_OK;
+}
+
 bool pdl_allowed(cudaStream_t s, LaunchClass cls) {
   static std::mutex mu;
   static std::unordered_map<cudaStream_t, int> last;  // class of the latest launch per stream
@@ -240,9 +249,7 @@ qg_status qffn_gate_up_silu(qg_type t, const void* qg, const uint16_t* sg, const
 }
 
 size_t qmoe_workspace_bytes(int n_expert, int ffn, int hidden, int ncols, int topk) {
-  if (n_expert < 1 || n_expert > QG_MOE_MAX_EXPERTS || ffn <= 0 || hidden <= 0 || ncols < 1 ||
-      ncols > 16 || topk < 1 || topk > 16)
-    return 0;
+  if (qg::moe_check_shape(QG_Q8_0, n_expert, ffn, hidden, ncols, topk) != QG_OK) return 0;
   return qg::moe_ws_bytes(n_expert, ffn, hidden, ncols, topk);
 }
 
@@ -253,10 +260,8 @@ qg_status qmoe_experts(qg_type t, const void* qg, const uint16_t* sg, const void
                        const uint16_t* x, int ncols, const float* y0, float* y,
                        void* ws, size_t ws_bytes, int32_t* err_flag,
                        int32_t* uniq_ids_out, cudaStream_t stream) {
-  if (!valid_type((int)t)) return QG_ERR_TYPE;
-  if (n_expert < 1 || n_expert > QG_MOE_MAX_EXPERTS || ffn <= 0 || hidden <= 0 || (ffn % 32) ||
-      (hidden % 32) || ncols < 1 || ncols > 16 || topk < 1 || topk > 16 || !qg::moe_shape_supported(ffn, hidden, ncols, topk))
-    return QG_ERR_SHAPE;
+  qg_status st0 = qg::moe_check_shape((int)t, n_expert, ffn, hidden, ncols, topk);
+  if (st0 != QG_OK) return st0;
   if (!qg || !sg || !qu || !su || !qd || !sd || !ids || !rw || !x || !y) return QG_ERR_NULL;
   const void* p16[] = {qg, sg, qu, su, qd, sd, x};
   for (const void* p : p16)

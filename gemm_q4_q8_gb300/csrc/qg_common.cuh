@@ -155,9 +155,9 @@ __device__ __forceinline__ Q8Word dequant_q8_word(uint32_t w) {
 // ------------------------------------------- programmatic dependent launch
 // Kernels of this library are launched with programmatic stream
 // serialisation: a kernel may start while the previous kernel on the stream is
-// finishing. pdl_trigger() lets the next kernel start early (the CUDA-core
-// kernels call it at their start; the tensor-core kernel never does, see
-// qg_tc.cu); pdl_wait() blocks
+// finishing. pdl_trigger() lets the next kernel start early (every kernel
+// calls it at its start; the host keeps a CUDA-core kernel from starting early
+// behind the tensor-core kernel, see LaunchClass in qg_internal.h); pdl_wait() blocks
 // until every earlier kernel on the stream has completed and its writes are
 // visible. Each kernel reads only weights (immutable inputs) before pdl_wait()
 // and touches activations, residuals, ids and outputs only after it. Launched

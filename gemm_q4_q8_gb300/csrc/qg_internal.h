@@ -118,6 +118,8 @@ struct MoeArgs {
 };
 size_t moe_ws_bytes(int n_expert, int ffn, int hidden, int ncols, int topk);
 bool moe_shape_supported(int ffn, int hidden, int ncols, int topk);
+// Type and shape checks of the MoE layer: QG_OK, QG_ERR_TYPE or QG_ERR_SHAPE.
+qg_status moe_check_shape(int t, int n_expert, int ffn, int hidden, int ncols, int topk);
 cudaError_t moe_forward(const MoeArgs& a, cudaStream_t s);
 
 cudaError_t repack_launch(int qt, const void* gguf, int rows, int k, void* q_out,

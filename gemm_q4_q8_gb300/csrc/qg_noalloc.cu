@@ -8,13 +8,18 @@
 // latency-critical loop where cudaMalloc (which may synchronise the device) is
 // not acceptable. For them this entry point uses a workspace that lives in the
 // library itself: a file-scope __device__ array of QG_MOE_NOALLOC_WS_BYTES,
-// which every GPU that loads this library holds until the process exits.
+// which every GPU that loads this library holds until the process exits. Its
+// size is the largest workspace any shape the MoE layer accepts can need, so
+// every accepted shape fits; a shape beyond it would get QG_ERR_WORKSPACE.
 //
 // The array name is only a host-side stand-in in host code, not a device
 // address. The first call on each device (with that device current) asks the
 // runtime for the array's device address with cudaGetSymbolAddress, checks the
 // result, and keeps the address for that device; later calls reuse it. That
-// first call should therefore come before any stream capture.
+// first call should therefore come before any stream capture. The kept address
+// belongs to the device's primary context: after cudaDeviceReset (or anything
+// else that destroys that context) it is stale, so this entry point must not
+// be used across a device reset.
 //
 // Every call shares the one array and it keeps the previous call's contents.
 // Nothing in it needs to start at zero: within a call, every workspace entry
@@ -69,12 +74,13 @@ extern "C" qg_status qmoe_experts_noalloc(qg_type t, const void* qg, const uint1
                                           const qg_expert* shared, const uint16_t* x, int ncols,
                                           const float* y0, float* y, int32_t* err_flag,
                                           int32_t* uniq_ids_out, cudaStream_t stream) {
-  const size_t need = qmoe_workspace_bytes(n_expert, ffn, hidden, ncols, topk);
-  if (need == 0) return QG_ERR_SHAPE;
-  if (need > kNoallocWsBytes) return QG_ERR_WORKSPACE;  // beyond the built-in maximum
-  void* ws = nullptr;
-  qg_status st = ws_address(&ws);
+  // The same type and shape checks as qmoe_experts, so both return the same status.
+  qg_status st = qg::moe_check_shape((int)t, n_expert, ffn, hidden, ncols, topk);
   if (st != QG_OK) return st;
+  if (qmoe_workspace_bytes(n_expert, ffn, hidden, ncols, topk) > kNoallocWsBytes)
+    return QG_ERR_WORKSPACE;  // beyond the built-in maximum (no accepted shape is)
+  void* ws = nullptr;
+  if ((st = ws_address(&ws)) != QG_OK) return st;
   return qmoe_experts(t, qg, sg, qu, su, qd, sd, n_expert, ffn, hidden, ids, rw, topk, shared, x,
                       ncols, y0, y, ws, kNoallocWsBytes, err_flag, uniq_ids_out, stream);
 }

@@ -143,7 +143,12 @@ qg_status qffn_gate_up_silu(qg_type t, const void *qg, const uint16_t *sg, const
  *                    y0 + sum_j rw[c][j] * D_e (SiLU(G_e x_c) * (U_e x_c)) + shared,
  *                    e = ids[c][j]; the intermediate h is rounded to f16.
  *   ws, ws_bytes   : device workspace of at least qmoe_workspace_bytes(...) bytes,
- *                    16-byte aligned; its contents on entry are ignored
+ *                    16-byte aligned; its contents on entry are ignored. When the
+ *                    call's work has completed, ws starts with the intermediate h
+ *                    of every (column, slot): f16 [ncols][topk + 1][ffn], slot
+ *                    topk being the shared expert; slots of invalid ids (and the
+ *                    shared slot when shared is NULL) hold unspecified values.
+ *                    A caller may read it to check the layer stage by stage.
  *   err_flag       : device int32 or NULL. An id outside [0, n_expert) makes that
  *                    slot contribute 0 and ORs QG_MOE_BAD_ID into *err_flag. The
  *                    library never clears the flag: zero it before the call and
@@ -164,6 +169,8 @@ typedef struct qg_expert {
 #define QG_MOE_BAD_ID 1
 #define QG_MOE_MAX_EXPERTS (1 << 22)
 
+/* Workspace bytes qmoe_experts needs for this shape; 0 for a shape that it
+ * rejects with QG_ERR_SHAPE. */
 size_t qmoe_workspace_bytes(int n_expert, int ffn, int hidden, int ncols, int topk);
 
 qg_status qmoe_experts(qg_type t, const void *qg, const uint16_t *sg, const void *qu,
@@ -182,15 +189,22 @@ qg_status qmoe_experts(qg_type t, const void *qg, const uint16_t *sg, const void
  * Arguments and results are those of qmoe_experts minus ws / ws_bytes; the
  * workspace is a QG_MOE_NOALLOC_WS_BYTES array inside the library, held on every
  * GPU that loads the library until the process exits.
- *  - Problems whose qmoe_workspace_bytes(...) exceeds QG_MOE_NOALLOC_WS_BYTES
- *    return QG_ERR_WORKSPACE before anything is launched.
+ *  - The array is as large as the largest workspace any shape qmoe_experts
+ *    accepts needs (16 columns x 32768 h values per column, f16), so every
+ *    accepted shape fits. Type and shape errors are those of qmoe_experts; a
+ *    problem whose qmoe_workspace_bytes(...) exceeded the array would get
+ *    QG_ERR_WORKSPACE before anything is launched.
  *  - The first call on each device (with that device current) looks up the
- *    array's device address; make that first call before any stream capture.
+ *    array's device address and keeps it; make that first call before any
+ *    stream capture. The kept address dies with the device's primary context:
+ *    do not use this call across cudaDeviceReset.
  *  - All calls share the array: calls whose GPU work overlaps (different
  *    streams, several host threads) race on it. Nothing in it needs clearing.
+ *  - After a call's work has completed the array holds that call's h, laid out
+ *    as qmoe_experts leaves it in its workspace.
  *  - Allocates nothing (no cudaMalloc, no library allocator).
  * ------------------------------------------------------------------------- */
-#define QG_MOE_NOALLOC_WS_BYTES ((size_t)8 << 20) /* 8 MiB */
+#define QG_MOE_NOALLOC_WS_BYTES ((size_t)1 << 20) /* 1 MiB */
 
 qg_status qmoe_experts_noalloc(qg_type t, const void *qg, const uint16_t *sg, const void *qu,
                                const uint16_t *su, const void *qd, const uint16_t *sd,

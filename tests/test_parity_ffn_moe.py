@@ -5,15 +5,20 @@ The f16 output h of the fused gate/up is checked against the oracle's f64
 SiLU(g) * u with the propagated bound of the GEMV tolerance through SiLU * up
 plus one f16 rounding. The down projection is checked twice: staged (the
 oracle takes the GPU's own f16 h as input, plain GEMV tolerance) and end to end
-(the oracle's f64 h, with the bound carried through). MoE routing (the ascending
-list of distinct experts) must match bit for bit.
+(the oracle's f64 h, with the bound carried through). The MoE layer is checked
+the same way: the h of every (column, slot) that the layer leaves in its
+workspace against the oracle's gate/up of that expert, then the down projection
+and weighted combine staged on the GPU's h (the check that sees a wrong routed
+combine at the layer's shape), then end to end. MoE routing (the ascending list
+of distinct experts) must match bit for bit.
 """
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from helpers import NTHREADS, assert_within, dev, dev_q, dev_u16, dev_u16_as_f16, gemv_bound, host
+from helpers import (NTHREADS, assert_within, check_moe_staged, dev, dev_q, dev_u16,
+                     dev_u16_as_f16, gemv_bound, host, workspace_h)
 
 pytestmark = pytest.mark.gpu
 
@@ -105,16 +110,17 @@ def gpu_moe(case, ids=None, with_y0=True, nshared=True):
                     dev_u16_as_f16(case["x"]), y, ws, y0=y0, shared=sh, err_flag=err,
                     uniq_ids_out=uniq)
     torch.cuda.synchronize()
-    return host(y), int(host(err)[0]), host(uniq)
+    return host(y), int(host(err)[0]), host(uniq), workspace_h(ws, case)
 
 
 def check_moe(case, ids=None, what=""):
-    y, err, uniq = gpu_moe(case, ids)
+    y, err, uniq, h_gpu = gpu_moe(case, ids)
     yr, bound, uref, nu, rc = oracle.moe(case, ids=ids, nthreads=NTHREADS)
     assert np.array_equal(uniq, uref), (what, uniq[:nu + 2], uref[:nu + 2])
     assert err == (1 if rc == 3 else 0)
     assert np.isfinite(y).all()
-    assert_within(y, yr, bound, what)
+    check_moe_staged(case, y, h_gpu, ids=ids, what=what)
+    assert_within(y, yr, bound, what + " (end to end)")
     return y, nu
 
 

@@ -165,6 +165,9 @@ def test_router_feeds_experts():
     assert np.array_equal(host(ids), rid)
     assert int(host(err)[0]) == 0
     ref_case = dict(case, ids=host(ids), rw=host(rw))
+    # stage by stage on the GPU's own h (left in the workspace), then end to end
+    from helpers import check_moe_staged, workspace_h
+    check_moe_staged(ref_case, host(y), workspace_h(ws, ref_case), what="router -> MoE experts")
     yr, bound, _, _, rc = oracle.moe(ref_case, nthreads=NTHREADS)
     assert rc == 0
-    assert_within(host(y), yr, bound, "router -> MoE experts")
+    assert_within(host(y), yr, bound, "router -> MoE experts (end to end)")

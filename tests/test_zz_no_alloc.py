@@ -1,9 +1,13 @@
 """qmoe_experts_noalloc: the MoE layer for callers that cannot allocate device
-memory (the workspace is an array inside the library). Checked through the C
-ABI against qmoe_experts with a caller-allocated workspace, on two calls in a
-row per case, within the MoE tolerance the other tests use (the oracle's
-propagated bound). This file is collected last so that a failure here stops a run only
-after every other test has run."""
+memory (a plugin inside a framework that owns every byte of device memory, a
+fixed memory budget, a loop that must not call cudaMalloc). Its workspace is an
+array inside the library. The GPU test calls it through the C ABI twice in a
+row per case, the second call finding the first call's contents in the shared
+array, and checks each output bit for bit against qmoe_experts with a
+caller-allocated workspace: both run the same kernels on the same shape, and
+the reduction order depends only on the shape. The oracle's MoE bound is kept
+as a second check. This file is collected last so that a failure here stops a
+run only after every other test has run."""
 import numpy as np
 import pytest
 
@@ -71,19 +75,36 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
         _, bound, _, _, _ = oracle.moe(case)
         for call in (1, 2):
             y_na, u_na, e_na = _run(case, a, noalloc=True)
-            assert np.isfinite(y_na).all()
-            assert_within(y_na, y_ws.astype(np.float64), bound, f"noalloc call {call} vs workspace")
+            assert np.array_equal(y_na.view(np.uint32), y_ws.view(np.uint32)), \
+                f"noalloc call {call} differs from the workspace call"
             assert np.array_equal(u_na, u_ws) and e_na == e_ws == 0
+            assert_within(y_na, oracle.moe(case)[0], bound, f"noalloc call {call} vs oracle")
 
 
-def test_noalloc_rejects_problems_beyond_its_workspace():
+def test_noalloc_workspace_holds_every_accepted_shape():
+    """The library's array is as large as the largest workspace any accepted
+    shape needs; shapes the MoE layer rejects get the same status from both
+    entry points (nothing is launched: the checks run on the host first)."""
     from gemm_q4_q8_gb300 import build
     build.build()
     L = qg.load()
-    # the workspace holds h for every (column, k) slot: a very wide expert FFN
-    # at 8 columns and top-16 exceeds 8 MiB
-    assert qg.qmoe_workspace_bytes(256, 32768, 1024, 8, 16) > qg.QG_MOE_NOALLOC_WS_BYTES
-    st = L.qmoe_experts_noalloc(8, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 256,
-                                32768, 1024, 0x10000, 0x10000, 16, None, 0x10000, 8, None,
-                                0x10000, None, None, None)
-    assert st == 5  # QG_ERR_WORKSPACE, nothing launched
+    # largest accepted: 16 columns, (topk + 1) * ffn = 32768 h values per column
+    biggest = qg.qmoe_workspace_bytes(256, 2048, 2048, 16, 15)
+    assert biggest == qg.QG_MOE_NOALLOC_WS_BYTES
+    assert qg.qmoe_workspace_bytes(256, 32768 // 17 // 32 * 32, 2048, 16, 16) <= biggest
+    # one step beyond in ffn, columns or top-k: rejected as a shape
+    assert qg.qmoe_workspace_bytes(256, 2048 + 32, 2048, 16, 15) == 0
+    assert qg.qmoe_workspace_bytes(256, 2048, 2048, 17, 15) == 0
+    assert qg.qmoe_workspace_bytes(256, 2048, 2048, 16, 16) == 0
+    p = 0x10000  # aligned, never dereferenced: the shape check comes first
+    for shape in ((256, 2048 + 32, 2048, 15, 16), (256, 32768, 1024, 16, 8)):
+        E, ffn, hidden, topk, ncols = shape
+        st_na = L.qmoe_experts_noalloc(qg.Q8_0, p, p, p, p, p, p, E, ffn, hidden, p, p, topk,
+                                       None, p, ncols, None, p, None, None, None)
+        st_ws = L.qmoe_experts(qg.Q8_0, p, p, p, p, p, p, E, ffn, hidden, p, p, topk, None, p,
+                               ncols, None, p, p, 1 << 30, None, None, None)
+        assert st_na == st_ws == qg.QG_ERR_SHAPE
+        assert L.qg_status_str(st_na).decode().startswith("invalid shape")
+    st = L.qmoe_experts_noalloc(3, p, p, p, p, p, p, 256, 512, 2048, p, p, 8, None, p, 1, None, p,
+                                None, None, None)
+    assert st == qg.QG_ERR_TYPE
