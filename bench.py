@@ -378,13 +378,17 @@ class ClockSampler:
 
 # ---------------------------------------------------------- CPU oracle
 def oracle_step_estimate(w: dict, frac: float, nthreads: int, h_for_down: np.ndarray) -> dict:
-    """Time the oracle on a fraction of every matrix of the step and scale each
-    part to the whole matrix: returns {kernel: seconds for the full kernel}."""
+    """Time the oracle on every matrix of the step (frac = 1: all rows, measured,
+    nothing scaled), or on an evenly spaced fraction of the rows of every dense
+    matrix, each part's time scaled to its whole matrix: returns {kernel:
+    seconds for the full kernel}. The MoE layer always runs whole."""
     import oracle
     oracle.build()
     est = {}
 
     def rows_sel(rows):
+        if frac >= 1.0:
+            return None, 1.0
         n = max(1, int(round(rows * frac)))
         return np.linspace(0, rows - 1, n).astype(np.int64), n / rows
 
@@ -408,8 +412,11 @@ def oracle_step_estimate(w: dict, frac: float, nthreads: int, h_for_down: np.nda
     ff = w["ffn"]
     sel, f = rows_sel(17408)
     # the oracle's fused gate/up computes every row; time it on a row slice
-    qg_s, sg_s = ff["qg"][sel], ff["sg"][sel]
-    qu_s, su_s = ff["qu"][sel], ff["su"][sel]
+    if sel is None:
+        qg_s, sg_s, qu_s, su_s = ff["qg"], ff["sg"], ff["qu"], ff["su"]
+    else:
+        qg_s, sg_s = ff["qg"][sel], ff["sg"][sel]
+        qu_s, su_s = ff["qu"][sel], ff["su"][sel]
     est["gateup"] = timed(lambda: oracle.ffn_gate_up_silu(ff["qtype"], qg_s, sg_s, qu_s, su_s,
                                                           ff["x"], nthreads=nthreads)) / f
     sel, f = rows_sel(5120)
@@ -420,22 +427,36 @@ def oracle_step_estimate(w: dict, frac: float, nthreads: int, h_for_down: np.nda
     return est
 
 
-def cpu_baseline(w: dict, wb: dict, frac: float = 1 / 64) -> dict:
-    nthreads = os.cpu_count() or 1
+def oracle_h_for_down() -> np.ndarray:
+    """f16 h [16][17408] fed to the oracle's down projection when it is timed
+    (the values do not change its work)."""
     g = synth.rng(77)
-    h = (g.standard_normal((16, 17408)) * 0.05).astype(np.float16).view(np.uint16)
-    est = oracle_step_estimate(w, frac, nthreads, h)
-    total_s = sum(est.values())
+    return (g.standard_normal((16, 17408)) * 0.05).astype(np.float16).view(np.uint16)
+
+
+def cpu_baseline(w: dict, wb: dict, passes: int = 2) -> dict:
+    """The oracle as it stands, timed on the whole step (every matrix, every
+    row, the whole MoE layer) on all host cores, `passes` times."""
+    nthreads = os.cpu_count() or 1
+    h = oracle_h_for_down()
+    times = []
+    parts = {}
+    for _ in range(passes):
+        est = oracle_step_estimate(w, 1.0, nthreads, h)
+        times.append(sum(est.values()))
+        parts = est
+    step_s = float(np.mean(times))
     return {
-        "value": sum(wb.values()) / total_s / 1e9,
+        "value": sum(wb.values()) / step_s / 1e9,
         "unit": UNIT,
         "cores": nthreads,
         "kind": "oracle",
-        "sample": (f"f64 C oracle with {nthreads} threads on {frac:.4f} of the rows of every "
-                   "dense matrix of the step (evenly spaced) and the whole MoE layer; each part's "
-                   "time scaled to its full matrix; value = step weight bytes / estimated step time"),
+        "sample": (f"f64 C oracle with {nthreads} threads on the whole step (every row of every "
+                   f"matrix, the whole MoE layer), {passes} passes, measured (nothing scaled); "
+                   "value = step weight bytes / mean pass time"),
         "cpu": platform.processor() or platform.machine(),
-        "est_step_s": total_s,
+        "step_s": step_s,
+        "part_s": {k: round(v, 4) for k, v in parts.items()},
     }
 
 
@@ -564,55 +585,94 @@ CONFIGS = (
     ("router_256x2048_top8_c8", "router", None, 256, 2048, 8, False),
     ("router_256x2048_top8_c16", "router", None, 256, 2048, 16, False),
 )
+# The configs the default bench line reports (the workload's configs at every
+# column count it names); --configs times all of CONFIGS.
+DEFAULT_CONFIGS = ("q8_gemv_2048_c1", "q4_gemv_5120_c1_y0", "q8_lmhead_248320_c1",
+                   "q4_twins_5120_c2", "q4_twins_5120_c4", "q4_twins_5120_c8",
+                   "q4_twins_17408_c2", "q4_twins_17408_c4", "q4_twins_17408_c8",
+                   "q8_twins_17408_c8", "q4_ffn_gateup_17408_c16",
+                   "q4_ffn_down_5120x17408_c16_y0", "q8_moe_c1", "q8_moe_c8", "q8_moe_c16")
 L2_BYTES = 129 * 2**20
 
 
-def run_configs(args):
+class ConfigTimer:
     """Each config of the workload alone: CUDA-graph replays of back-to-back
-    calls that cycle through enough distinct weight copies (>= 4x L2, or one
-    copy when a single one is larger) that L2 holds none of them; MoE calls
-    cycle through 8 id sets. 20 warm-up calls; per replay, the mean call time;
-    median and p10/p90 over the replays. Beside it, the oracle's time per
-    call (rows sampled and scaled; 1 thread and all host threads). One JSON
-    line per config."""
-    import torch
-    import gemm_q4_q8_gb300 as qg
-    import oracle
-    from gemm_q4_q8_gb300 import build
-    build.build()
-    oracle.build()
-    peak, peak_kind = peaks()
-    stream = torch.cuda.current_stream()
-    ncores = os.cpu_count() or 1
+    calls that cycle through enough distinct weight copies (>= 4x L2, at most
+    16, or one copy when a single one is larger) that L2 holds none of them;
+    MoE calls cycle through 8 id sets. 20 warm-up calls; per replay, the mean
+    call time; median and p10/p90 over the replays.
 
-    def d(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    Device matrices come from the step's own buffers where the step has the
+    same matrix (rotating copies are device-to-device clones of it); the rest
+    are drawn with the same distributions and repacked on the GPU."""
 
-    def dq(qtype, q, scl):
+    def __init__(self, torch, qg, gs, w):
+        self.t, self.qg, self.gs, self.w = torch, qg, gs, w
+        self.stream = torch.cuda.current_stream()
+
+    def d(self, a):
+        return self.t.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def dq(self, qtype, q, scl):
+        t = self.t
         rows, nb = scl.shape
-        blocks = d(synth.to_gguf_blocks(qtype, q, scl))
-        qd = torch.empty(q.shape, dtype=torch.uint8, device="cuda")
-        sd = torch.empty(scl.shape, dtype=torch.int16, device="cuda")
-        qg.qrepack(qtype, blocks, rows, nb * 32, qd, sd)
-        torch.cuda.synchronize()
+        blocks = self.d(synth.to_gguf_blocks(qtype, q, scl))
+        qd = t.empty(q.shape, dtype=t.uint8, device="cuda")
+        sd = t.empty(scl.shape, dtype=t.int16, device="cuda")
+        self.qg.qrepack(qtype, blocks, rows, nb * 32, qd, sd)
+        t.cuda.synchronize()
         return qd, sd
 
-    def oracle_us(fn, frac):
-        t0 = time.perf_counter()
-        fn()
-        return (time.perf_counter() - t0) / frac * 1e6
+    def host_matrices(self, kind, qt, rows, k):
+        """Host (quants, scales) of the config's matrices, from the workload
+        when it holds that matrix; None when it must be drawn."""
+        w = self.w
+        if w is None:
+            return None
+        if kind == "gateup" and (qt, rows, k) == (synth.Q4_0, 17408, 5120) and "ffn" in w:
+            f = w["ffn"]
+            return [(f["qg"], f["sg"]), (f["qu"], f["su"])]
+        if kind == "cols" and (qt, rows, k) == (synth.Q4_0, 5120, 17408) and "ffn" in w:
+            return [(w["ffn"]["qd"], w["ffn"]["sd"])]
+        if kind == "gemv":
+            for key in ("gemv", "lmhead", "twins"):
+                c = w.get(key)
+                if c is not None and (c["qtype"], c["scl"].shape[0], c["k"]) == (qt, rows, k):
+                    return [(c["q"], c["scl"])]
+        return None
 
-    for name, kind, qt, rows, k, ncols, residual in CONFIGS:
-        if args.config_filter and args.config_filter not in name:
-            continue
+    def device_matrix(self, kind, qt, rows, k, mats):
+        """Device copies of the config's matrices: the step's own when it has
+        them, else repacked from `mats`."""
+        gs = self.gs
+        if gs is not None:
+            if kind == "gateup" and hasattr(gs, "f_qg") and (qt, rows, k) == (synth.Q4_0, 17408, 5120):
+                return [(gs.f_qg, gs.f_sg), (gs.f_qu, gs.f_su)]
+            if kind == "cols" and hasattr(gs, "f_qd") and (qt, rows, k) == (synth.Q4_0, 5120, 17408):
+                return [(gs.f_qd, gs.f_sd)]
+            if kind == "gemv":
+                for key, attr in (("gemv", "g"), ("lmhead", "l"), ("twins", "t")):
+                    c = self.w.get(key) if self.w else None
+                    if (c is not None and hasattr(gs, attr + "_q") and
+                            (c["qtype"], c["scl"].shape[0], c["k"]) == (qt, rows, k)):
+                        return [(getattr(gs, attr + "_q"), getattr(gs, attr + "_s"))]
+        return [self.dq(qt, q, sc) for (q, sc) in mats]
+
+    def build(self, name, kind, qt, rows, k, ncols, residual, with_oracle):
+        """(calls, weight bytes, total bytes, oracle fns or None, oracle row
+        fraction, extra keys) of one config."""
+        t, qg = self.t, self.qg
         g = synth.rng(1)
         calls = []
+        ncores = os.cpu_count() or 1
+        o_fn, o_frac = None, 1.0
+        import oracle
         if kind in ("argmax", "topk"):
             n, kk = rows, k
             xs_np = [g.standard_normal((ncols, n)).astype(np.float32) for _ in range(4)]
-            xs_d = [d(a) for a in xs_np]
-            ib = torch.empty((ncols, kk), dtype=torch.int32, device="cuda")
-            vb = torch.empty((ncols, kk), dtype=torch.float32, device="cuda")
+            xs_d = [self.d(a) for a in xs_np]
+            ib = t.empty((ncols, kk), dtype=t.int32, device="cuda")
+            vb = t.empty((ncols, kk), dtype=t.float32, device="cuda")
             for a in xs_d:
                 if kind == "argmax":
                     calls.append(lambda s, a=a: qg.qargmax_f32(a, ib[:, 0], vb[:, 0], s))
@@ -620,18 +680,18 @@ def run_configs(args):
                     calls.append(lambda s, a=a: qg.qtopk_f32(a, kk, ib, vb, s))
             wbytes = ncols * n * 4  # logits read (no weights)
             tbytes = wbytes + ncols * kk * 8  # + indices and values written
-            o_frac = 1.0
-            o_fn = {t: ((lambda: oracle.argmax(xs_np[0])) if kind == "argmax"
-                        else (lambda: oracle.topk(xs_np[0], kk))) for t in (1, ncores)}
+            if with_oracle:
+                o_fn = {th: ((lambda: oracle.argmax(xs_np[0])) if kind == "argmax"
+                             else (lambda: oracle.topk(xs_np[0], kk))) for th in (1, ncores)}
             extra = {"bytes_are": "logits read", "k": kk}
         elif kind == "router":
             E, hid = rows, k
             wr_np = [(g.standard_normal((E, hid)) * 0.02).astype(np.float32) for _ in range(4)]
             x_np = synth.draw_x(g, ncols, hid)
-            wr = [d(a) for a in wr_np]
-            x = d(x_np.view(np.int16)).view(torch.float16)
-            ib = torch.empty((ncols, 8), dtype=torch.int32, device="cuda")
-            rb = torch.empty((ncols, 8), dtype=torch.float32, device="cuda")
+            wr = [self.d(a) for a in wr_np]
+            x = self.d(x_np.view(np.int16)).view(t.float16)
+            ib = t.empty((ncols, 8), dtype=t.int32, device="cuda")
+            rb = t.empty((ncols, 8), dtype=t.float32, device="cuda")
             for a in wr:
                 calls.append(lambda s, a=a: qg.qmoe_router(a, x, 8, ib, rb, stream=s))
             wbytes = E * hid * 4  # f32 router weights
@@ -641,54 +701,64 @@ def run_configs(args):
                 lg, _ = oracle.router_logits(wr_np[i], x_np)
                 _, v = oracle.topk(lg.astype(np.float32), 8)
                 return [oracle.softmax(r) for r in v]
-            o_frac = 1.0
-            o_fn = {t: o_router for t in (1, ncores)}
+            if with_oracle:
+                o_fn = {th: o_router for th in (1, ncores)}
             extra = {"bytes_are": "f32 router weights", "topk": 8}
         elif kind == "moe":
-            m = synth.moe_layer(ncols, seed=2)
-            dm = {}
-            for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
-                dm[a], dm[b] = dq(qt, m[a], m[b])
-            sh = {}
-            for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
-                sh[a], sh[b] = dq(qt, m["shared"][a], m["shared"][b])
-            ws = torch.empty(qg.qmoe_workspace_bytes(256, 512, 2048, ncols, 8), dtype=torch.uint8,
-                             device="cuda")
+            gs = self.gs
+            m_host = self.w["moe"] if (self.w is not None and "moe" in self.w) else synth.moe_layer(8, seed=2)
+            if gs is not None and hasattr(gs, "m"):
+                dm, sh = gs.m, gs.m_sh
+            else:
+                dm, sh = {}, {}
+                for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd")):
+                    dm[a], dm[b] = self.dq(qt, m_host[a], m_host[b])
+                    sh[a], sh[b] = self.dq(qt, m_host["shared"][a], m_host["shared"][b])
+            E, ffn, hid = m_host["n_expert"], m_host["ffn"], m_host["hidden"]
+            ws = t.empty(qg.qmoe_workspace_bytes(E, ffn, hid, ncols, 8), dtype=t.uint8,
+                         device="cuda")
             gi = synth.rng(9)
-            idn = [np.stack([gi.choice(256, 8, replace=False) for _ in range(ncols)]).astype(np.int32)
+            idn = [np.stack([gi.choice(E, 8, replace=False) for _ in range(ncols)]).astype(np.int32)
                    for _ in range(8)]
+            x_np = synth.draw_x(gi, ncols, hid)
+            _, rw_np = synth.draw_routing(gi, ncols, E, 8)
             uniq = float(np.mean([len(np.unique(i)) for i in idn]))
-            wbytes = (uniq + 1) * 3 * synth.weight_bytes(qt, 512, 2048)
+            wbytes = (uniq + 1) * 3 * synth.weight_bytes(qt, ffn, hid)
             # + x, y, ids, rw, and h (f16 [ncols][9][512]) written then read
-            tbytes = wbytes + ncols * 2048 * (2 + 4) + ncols * 8 * 8 + 2 * ncols * 9 * 512 * 2
-            ids = [d(i) for i in idn]
-            rw, x = d(m["rw"]), d(m["x"].view(np.int16)).view(torch.float16)
-            y = torch.empty((ncols, 2048), dtype=torch.float32, device="cuda")
+            tbytes = wbytes + ncols * hid * (2 + 4) + ncols * 8 * 8 + 2 * ncols * 9 * ffn * 2
+            ids = [self.d(i) for i in idn]
+            rw, x = self.d(rw_np), self.d(x_np.view(np.int16)).view(t.float16)
+            y = t.empty((ncols, hid), dtype=t.float32, device="cuda")
             for i in range(8):
                 calls.append(lambda s, i=i: qg.qmoe_experts(
-                    qt, dm["qg"], dm["sg"], dm["qu"], dm["su"], dm["qd"], dm["sd"], 256, 512, 2048,
+                    qt, dm["qg"], dm["sg"], dm["qu"], dm["su"], dm["qd"], dm["sd"], E, ffn, hid,
                     ids[i], rw, x, y, ws, shared=sh, stream=s))
-            o_frac = 1.0
-            o_fn = {t: (lambda t=t: oracle.moe(m, nthreads=t)) for t in (1, ncores)}
+            if with_oracle:
+                mc = dict(m_host, ncols=ncols, ids=idn[0], rw=rw_np, x=x_np, y0=None)
+                o_fn = {th: (lambda th=th: oracle.moe(mc, nthreads=th)) for th in (1, ncores)}
             extra = {"distinct_experts_mean": uniq}
         else:
             nmat = 2 if kind == "gateup" else 1
             wb1 = nmat * synth.weight_bytes(qt, rows, k)
             ncopy = int(min(16, max(1, np.ceil(4 * L2_BYTES / wb1))))
-            mats = [synth.draw_matrix(g, qt, rows, k) for _ in range(nmat)]
+            mats = self.host_matrices(kind, qt, rows, k)
+            if mats is None:
+                mats = [synth.draw_matrix(g, qt, rows, k) for _ in range(nmat)]
             x_np = synth.draw_x(g, ncols, k)
             y0_np = synth.draw_y0(g, ncols, rows) if residual else None
-            dev_mats = [[dq(qt, q, sc) for (q, sc) in mats] for _ in range(ncopy)]
-            x = d(x_np.view(np.int16)).view(torch.float16)
-            y0 = d(y0_np) if residual else None
+            first = self.device_matrix(kind, qt, rows, k, mats)
+            dev_mats = [first] + [[(a.clone(), sa.clone()) for (a, sa) in first]
+                                  for _ in range(ncopy - 1)]
+            x = self.d(x_np.view(np.int16)).view(t.float16)
+            y0 = self.d(y0_np) if residual else None
             if kind == "gateup":
-                h = torch.empty((ncols, rows), dtype=torch.float16, device="cuda")
+                h = t.empty((ncols, rows), dtype=t.float16, device="cuda")
                 for c in range(ncopy):
                     (a, sa), (b, sb) = dev_mats[c]
                     calls.append(lambda s, a=a, sa=sa, b=b, sb=sb: qg.qffn_gate_up_silu(
                         qt, a, sa, b, sb, x, h, s))
             else:
-                y = torch.empty((ncols, rows), dtype=torch.float32, device="cuda")
+                y = t.empty((ncols, rows), dtype=t.float32, device="cuda")
                 fn = qg.qgemm_cols if kind == "cols" else (
                     qg.qgemv_q4_0 if qt == synth.Q4_0 else qg.qgemv_q8_0)
                 for c in range(ncopy):
@@ -701,61 +771,102 @@ def run_configs(args):
             # + x read, y (f32) or h (f16) written, y0 read
             out_b = ncols * rows * (2 if kind == "gateup" else 4)
             tbytes = wbytes + ncols * k * 2 + out_b + (ncols * rows * 4 if residual else 0)
-            # the oracle runs on an evenly spaced row sample of about 25 M weights
-            # (the whole matrix when it is smaller), its time scaled to all rows
-            n_s = max(1, min(rows, int(25e6 / (nmat * k))))
-            sel = np.linspace(0, rows - 1, n_s).astype(np.int64)
-            o_frac = n_s / rows
-            if kind == "gateup":
-                (q1, s1), (q2, s2) = mats
-                o_fn = {t: (lambda t=t: oracle.ffn_gate_up_silu(qt, q1[sel], s1[sel], q2[sel], s2[sel],
-                                                                x_np, nthreads=t)) for t in (1, ncores)}
-            else:
-                (q1, s1), = mats
-                o_fn = {t: (lambda t=t: oracle.matmul(qt, q1, s1, x_np, y0_np, rows_sel=sel,
-                                                      nthreads=t)) for t in (1, ncores)}
+            if with_oracle:
+                # the oracle runs on an evenly spaced row sample of about 25 M
+                # weights (the whole matrix when it is smaller), scaled to all rows
+                n_s = max(1, min(rows, int(25e6 / (nmat * k))))
+                sel = np.linspace(0, rows - 1, n_s).astype(np.int64)
+                o_frac = n_s / rows
+                if kind == "gateup":
+                    (q1, s1), (q2, s2) = mats
+                    o_fn = {th: (lambda th=th: oracle.ffn_gate_up_silu(
+                        qt, q1[sel], s1[sel], q2[sel], s2[sel], x_np, nthreads=th))
+                        for th in (1, ncores)}
+                else:
+                    (q1, s1), = mats
+                    o_fn = {th: (lambda th=th: oracle.matmul(qt, q1, s1, x_np, y0_np, rows_sel=sel,
+                                                           nthreads=th)) for th in (1, ncores)}
             extra = {"weight_copies": ncopy}
-        # graph of back-to-back calls cycling the copies
+        return calls, wbytes, tbytes, o_fn, o_frac, extra
+
+    def time_calls(self, calls):
+        """Per-call µs of back-to-back graph replays: (median, p10, p90, calls timed)."""
+        t = self.t
         reps = max(len(calls), 16)
-        gcap = torch.cuda.Stream()
-        with torch.cuda.stream(gcap):
+        gcap = t.cuda.Stream()
+        with t.cuda.stream(gcap):
             for i in range(20):
                 calls[i % len(calls)](gcap)
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=gcap):
+        t.cuda.synchronize()
+        graph = t.cuda.CUDAGraph()
+        with t.cuda.graph(graph, stream=gcap):
             for i in range(reps):
                 calls[i % len(calls)](gcap)
         for _ in range(3):
             graph.replay()
-        torch.cuda.synchronize()
+        t.cuda.synchronize()
         nrep = max(13, -(-200 // reps))
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        evs = [(t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True))
                for _ in range(nrep)]
         for e0, e1 in evs:
-            e0.record(stream)
+            e0.record(self.stream)
             graph.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
+            e1.record(self.stream)
+        t.cuda.synchronize()
         per_call = np.array([e0.elapsed_time(e1) * 1e3 / reps for e0, e1 in evs])
-        med = float(np.median(per_call))
-        o1 = oracle_us(o_fn[1], o_frac)
-        on = oracle_us(o_fn[ncores], o_frac)
-        line = {
-            "config": name, "us_median": med,
-            "us_p10": float(np.percentile(per_call, 10)), "us_p90": float(np.percentile(per_call, 90)),
-            "timed_calls": int(nrep * reps), "weight_bytes": wbytes,
-            "total_bytes": tbytes,
-            "GBps": wbytes / (med * 1e-6) / 1e9,
-            "frac_of_measured_hbm": wbytes / (med * 1e-6) / 1e9 / peak, "peak_kind": peak_kind,
-            "frac_of_8TBps_nominal": wbytes / (med * 1e-6) / 8e12,
-            "oracle_us_1thread": o1, "oracle_us_all_threads": on, "oracle_threads": ncores,
-            "oracle_sample": ("whole layer" if kind == "moe" else f"{o_frac:.3f} of the rows, scaled"),
-        }
-        line.update(extra)
+        del graph
+        return (float(np.median(per_call)), float(np.percentile(per_call, 10)),
+                float(np.percentile(per_call, 90)), int(nrep * reps))
+
+    def run(self, names, with_oracle, peak, peak_kind):
+        """One dict per config name (in CONFIGS order)."""
+        out = []
+        ncores = os.cpu_count() or 1
+        for name, kind, qt, rows, k, ncols, residual in CONFIGS:
+            if name not in names:
+                continue
+            calls, wbytes, tbytes, o_fn, o_frac, extra = self.build(
+                name, kind, qt, rows, k, ncols, residual, with_oracle)
+            med, p10, p90, ncalls = self.time_calls(calls)
+            line = {"config": name, "us_median": med, "us_p10": p10, "us_p90": p90,
+                    "timed_calls": ncalls, "weight_bytes": wbytes, "total_bytes": tbytes,
+                    "GBps": wbytes / (med * 1e-6) / 1e9,
+                    "frac_of_measured_hbm": wbytes / (med * 1e-6) / 1e9 / peak,
+                    "peak_kind": peak_kind,
+                    "frac_of_8TBps_nominal": wbytes / (med * 1e-6) / 8e12}
+            if o_fn is not None:
+                def oracle_us(fn):
+                    t0 = time.perf_counter()
+                    fn()
+                    return (time.perf_counter() - t0) / o_frac * 1e6
+                line.update({"oracle_us_1thread": oracle_us(o_fn[1]),
+                             "oracle_us_all_threads": oracle_us(o_fn[ncores]),
+                             "oracle_threads": ncores,
+                             "oracle_sample": ("whole layer" if kind == "moe" else
+                                               f"{o_frac:.3f} of the rows, scaled")})
+            line.update(extra)
+            out.append(line)
+            del calls
+            self.t.cuda.empty_cache()
+        return out
+
+
+def run_configs(args):
+    """Every config of CONFIGS alone (ConfigTimer), with the oracle's time per
+    call beside it (rows sampled and scaled; 1 thread and all host threads).
+    One JSON line per config."""
+    import torch
+    import gemm_q4_q8_gb300 as qg
+    import oracle
+    from gemm_q4_q8_gb300 import build
+    build.build()
+    oracle.build()
+    peak, peak_kind = peaks()
+    names = [c[0] for c in CONFIGS if not args.config_filter or args.config_filter in c[0]]
+    w = make_workload(0)
+    gs = GpuStep(w, torch)
+    for line in ConfigTimer(torch, qg, gs, w).run(names, True, peak, peak_kind):
         print(json.dumps(line), flush=True)
-        del calls, graph
-        torch.cuda.empty_cache()
     return 0
 
 
@@ -769,8 +880,7 @@ def run_reference(args):
     wb = weight_bytes(w, uniq)
     frac = args.ref_frac
     nthreads = os.cpu_count() or 1
-    g = synth.rng(77)
-    h = (g.standard_normal((16, 17408)) * 0.05).astype(np.float16).view(np.uint16)
+    h = oracle_h_for_down()
     for _ in range(args.warmup):
         oracle_step_estimate(w, frac, nthreads, h)
     times = []
@@ -785,8 +895,11 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
-                         "sample": f"{frac:.4f} of the rows of every dense matrix per step, "
-                                   "whole MoE layer; times scaled to full matrices"},
+                         "sample": ("each step one whole pass of the oracle over the step "
+                                    "(every row of every matrix, the whole MoE layer), measured"
+                                    if frac >= 1.0 else
+                                    f"{frac:.4f} of the rows of every dense matrix per step, "
+                                    "whole MoE layer; times scaled to full matrices")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -797,11 +910,13 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     # default: 1000 device steps (~0.3 s timed, several clock samples); the
-    # reference arm's steps are oracle passes of ~0.25 s each, so 20 there
+    # reference arm's steps are whole oracle passes of ~1.2 s each, so 20 there
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--ref-frac", type=float, default=1 / 256)
+    ap.add_argument("--ref-frac", type=float, default=1.0,
+                    help="fraction of the rows the reference arm's oracle runs (1: all)")
+    ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=KERNELS + EXTRA_CASES, default=None,
                     help="profiling target: run only this call (see run_case)")
@@ -885,6 +1000,15 @@ def main(argv=None):
     launches = launches_per_step * args.steps
     if world > 1:
         torch.distributed.barrier()
+    # A second window of about a second of back-to-back step replays (not part
+    # of the timed region), so the clock record has samples under this load
+    # however short the timed region is.
+    n_sus = int(max(1, min(20000, 1.0 / max(e0.elapsed_time(e1) * 1e-3 / args.steps, 1e-6))))
+    t_sus0 = time.time()
+    for i in range(n_sus):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    t_sus1 = time.time()
     clk.stop()
     ms_per_step, value = whole_job_rate(step_bytes, e0.elapsed_time(e1), args.steps, world,
                                         torch, device)
@@ -974,7 +1098,25 @@ def main(argv=None):
                   "host memory on a copy stream (two device buffer sets, so one step's copies "
                   "overlap the neighbouring step's kernels), all inside the timed region",
         "clocks": clk.summary(t_wall0, t_wall1),
+        "clocks_sustained": dict(clk.summary(t_sus0, t_sus1), steps=n_sus,
+                                 note="untimed window of back-to-back step replays right "
+                                      "after the timed region"),
     }
+    if rank == 0 and not args.no_per_config:
+        # every workload config alone, graph replays over rotating weight copies
+        del graphs
+        torch.cuda.empty_cache()
+        pc = ConfigTimer(torch, qg, gs, w).run(DEFAULT_CONFIGS, False, peak, peak_kind)
+        line["per_config"] = {
+            d["config"]: {"us": round(d["us_median"], 3), "us_p10": round(d["us_p10"], 3),
+                          "us_p90": round(d["us_p90"], 3), "weight_bytes": d["weight_bytes"],
+                          "GBps": round(d["GBps"], 1),
+                          "frac_of_measured_hbm": round(d["frac_of_measured_hbm"], 4)}
+            for d in pc}
+        line["per_config_timing"] = ("each config alone: CUDA-graph replays of back-to-back "
+                                     "calls cycling through distinct weight copies (>= 4x L2, "
+                                     "at most 16; one when a copy is larger) and 8 MoE id sets; "
+                                     "median per call over >= 13 replays")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, wb)
     if rank == 0:

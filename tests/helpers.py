@@ -130,7 +130,8 @@ def check_moe_staged(case, y, h_gpu, ids=None, what=""):
     a wrong expert exceed."""
     import oracle
     href, hb, valid = moe_slot_h(case, ids=ids, nthreads=NTHREADS)
-    got_h = h_gpu.view(np.float16).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # slots of invalid ids hold unwritten bytes
+        got_h = h_gpu.view(np.float16).astype(np.float64)
     assert np.isfinite(got_h[valid]).all(), what
     assert_within(got_h[valid], href[valid], hb[valid], what + " h per slot")
     ys, bs, _, _, _ = oracle.moe(case, h_in=h_gpu, ids=ids, nthreads=NTHREADS)
