@@ -515,10 +515,12 @@ def run_case(args):
 
 # The next steps around the step's calls, as single-kernel profiling targets
 # at their config sizes: greedy argmax and top-40 over one column of 248,320
-# logits; the MoE router (256 x 2048 f32, top-8) on one column; and the small
+# logits; the MoE router (256 x 2048 f32, top-8) on one column; the small
 # Q8_0 decode GEMV (2048 x 2048, one column, CUDA-core kernel), which the step
-# does not contain.
-EXTRA_CASES = ("argmax", "topk40", "router", "q8gemv2048")
+# does not contain; and a tall Q4_0 / Q8_0 matrix (--case-rows rows, default
+# 65,536, by 5,120; --case-cols columns, default 8), where the tensor-core
+# kernel streams long enough to show its steady state.
+EXTRA_CASES = ("argmax", "topk40", "router", "q8gemv2048", "q4tall", "q8tall")
 
 
 def run_extra_case(args, torch, qg):
@@ -534,6 +536,19 @@ def run_extra_case(args, torch, qg):
                 qg.qargmax_f32(x, idx[:, 0], val[:, 0], stream)
             else:
                 qg.qtopk_f32(x, k, idx, val, stream)
+    elif args.case in ("q4tall", "q8tall"):
+        qt = synth.Q4_0 if args.case == "q4tall" else synth.Q8_0
+        c = synth.gemv_case(qt, args.case_rows or 65536, 5120, args.case_cols or 8,
+                            residual=False, seed=5)
+        blocks = torch.from_numpy(synth.to_gguf_blocks(qt, c["q"], c["scl"])).cuda()
+        q = torch.empty(c["q"].shape, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(c["scl"].shape, dtype=torch.int16, device="cuda")
+        qg.qrepack(qt, blocks, c["rows"], c["k"], q, sc)
+        x = torch.from_numpy(c["x"].view(np.int16)).cuda().view(torch.float16)
+        y = torch.empty((c["ncols"], c["rows"]), dtype=torch.float32, device="cuda")
+        fn = qg.qgemv_q4_0 if qt == synth.Q4_0 else qg.qgemv_q8_0
+        for _ in range(args.steps):
+            fn(q, sc, x, y, None, stream)
     elif args.case == "q8gemv2048":
         c = synth.small_q8_gemv()
         blocks = torch.from_numpy(synth.to_gguf_blocks(c["qtype"], c["q"], c["scl"])).cuda()
@@ -921,6 +936,7 @@ def main(argv=None):
     ap.add_argument("--case", choices=KERNELS + EXTRA_CASES, default=None,
                     help="profiling target: run only this call (see run_case)")
     ap.add_argument("--case-rows", type=int, default=0)
+    ap.add_argument("--case-cols", type=int, default=0)
     ap.add_argument("--configs", action="store_true",
                     help="time every workload config alone (one JSON line each)")
     ap.add_argument("--config-filter", default="")

@@ -23,12 +23,11 @@ template <> struct QTraits<T_Q8_0> { static constexpr int QB = 32; };
 constexpr uint32_t MAGIC_2P23 = 0x4B000000u;
 constexpr float F_2P23 = 8388608.0f;
 
-// The same pattern (and 1024 twice as f16x2) in constant memory. Read from
-// there, the pattern reaches the dequantisers as a register that the compiler
-// cannot fold into an immediate, so each (w & mask) | pattern below stays one
-// three-input logic instruction (a logic op takes one immediate at most).
+// The same pattern in constant memory. Read from there, the pattern reaches the
+// dequantisers as a register that the compiler cannot fold into an immediate,
+// so each (w & mask) | pattern below stays one three-input logic instruction
+// (a logic op takes one immediate at most).
 static __constant__ uint32_t c_or_f32 = 0x4B000000u;
-static __constant__ uint32_t c_or_f16x2 = 0x64006400u;
 
 // (a & MASK) | orv as one lop3 (truth table 0xEA = (A & B) | C).
 template <uint32_t MASK>

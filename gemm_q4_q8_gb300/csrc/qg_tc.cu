@@ -41,11 +41,9 @@ namespace qg {
 
 constexpr int TC_BM = 64;                 // rows per CTA
 constexpr int TC_KT = 256;                // weights per stage (one K unit)
-constexpr int TC_CONSUMERS = 8;           // 4 m-tiles x 2 k-groups
-constexpr int TC_WARP_TMA = TC_CONSUMERS;  // issues the TMA copies
-constexpr int TC_THREADS = (TC_CONSUMERS + 1) * 32;
 constexpr int TC_SMEM_BUDGET = 112 * 1024;  // two CTAs per SM
 constexpr long long TC_WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before giving up
+constexpr uint32_t TC_SUSPEND_NS = 1000000;        // suspend-time hint of one try_wait (1 ms)
 
 __device__ int32_t g_tc_error = 0;        // QG_DEV_ERR_WAIT: a wait timed out
 
@@ -56,28 +54,34 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+// Arrive once per warp, from lane 0, without a divergent branch.
+__device__ __forceinline__ void mbar_arrive_lane0(uint32_t bar, int lane) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %1, 0;\n\t"
+      "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar), "r"(lane)
+      : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One try_wait on a phase: the warp may be parked until the phase completes
+// (or the hint runs out), so a wait on a stage that is not ready yet costs no
+// polling loop.
+__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(TC_SUSPEND_NS)
       : "memory");
-  return ok != 0;
+  return ok;
 }
-// Bounded wait on a phase of an mbarrier; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The rest of a wait whose first try failed: bounded by the clock (~2 s), after
+// which the error bit is set and the caller falls through.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > TC_WAIT_LIMIT) {
@@ -87,12 +91,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
   return true;
 }
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar, uint64_t policy) {
+// Bounded wait on a phase of an mbarrier; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity);
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -106,22 +114,28 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ uint16_t lds16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
+}
+// Two f16 scales packed in a word, as f32 (the conversion reads each half in
+// place, no extraction).
+__device__ __forceinline__ float lo_f32(uint32_t w) {
+  return __low2float(*reinterpret_cast<const __half2*>(&w));
+}
+__device__ __forceinline__ float hi_f32(uint32_t w) {
+  return __high2float(*reinterpret_cast<const __half2*>(&w));
 }
 // D = A * B (+ C), f16 inputs, f32 accumulate.
+// The mma are pure register operations (not volatile): the compiler may
+// interleave them with the dequantisation of the next block.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%10, %11, %12, %13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -130,7 +144,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 }
 __device__ __forceinline__ void mma16816_acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                              uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -151,10 +165,10 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) 
 // 2t, 2t+8, 2t+1, 2t+9 (GGUF byte j holds element j low, j+16 high). 0x6400 is
 // f16 1024 (one mantissa step = 1). Results, each equal to (q - 8) exactly:
 //   e0 = (el 2t, 2t+1), e2 = (2t+8, 2t+9), e1 = (2t+16, 2t+17), e3 = (2t+24, 2t+25)
-__device__ __forceinline__ void dq4_f16(uint32_t w, uint32_t& e0, uint32_t& e1, uint32_t& e2,
-                                        uint32_t& e3) {
+// M: the pattern 0x64006400 (f16 1024 twice), held in a register.
+__device__ __forceinline__ void dq4_f16(uint32_t w, uint32_t M, uint32_t& e0, uint32_t& e1,
+                                        uint32_t& e2, uint32_t& e3) {
   const uint32_t w8 = w >> 8;
-  const uint32_t M = c_or_f16x2;
   const uint32_t k1032 = 0x64086408u;  // 1032 = 1024 + 8
   const uint32_t k16th = 0x2C002C00u;  // 1/16
   const uint32_t km72 = 0xD480D480u;   // -72
@@ -184,8 +198,18 @@ struct TcParams {
   __half* h;
 };
 
+// KG k-groups of consumer warps split a unit's 8 blocks (8 / KG blocks per warp
+// and unit); 4 m-tiles x KG k-groups of consumers plus one TMA producer warp.
+// (4 k-groups, 16 consumer warps with half the work each, measured slower:
+// every warp pays the per-stage waits and address work, and the instruction
+// count per weight rose by half. Two units per stage behind one pair of
+// barriers measured no faster.)
 template <int QT, int NT, bool DUAL>
 struct TcShape {
+  static constexpr int KG = 2;
+  static constexpr int BPW = 8 / KG;                     // blocks per warp and unit
+  static constexpr int CONS = 4 * KG;                    // consumer warps
+  static constexpr int THREADS = (CONS + 1) * 32;        // + the producer warp (last)
   static constexpr int NMAT = DUAL ? 2 : 1;
   static constexpr int QROW = QT == T_Q4_0 ? 128 : 256;  // quant bytes per row per unit
   static constexpr int A_BYTES = TC_BM * QROW;
@@ -194,12 +218,18 @@ struct TcShape {
   static constexpr int CPAD = 8 * NT;
   static constexpr int X_BYTES = CPAD * TC_KT * 2;       // x of one unit (TMA), [4][CPAD][64] f16
   static constexpr int STAGE = AS_BYTES + X_BYTES;
+  // Release a stage as soon as its bytes are in registers (before the
+  // arithmetic) on the memory-bound plan, the single-matrix Q8_0 one: its
+  // refill then overlaps this stage's arithmetic (measured: Q8_0 LM head 192
+  // -> 188.6 us). Where the arithmetic is the bound (Q4_0, fused gate/up) the
+  // release stays after it: releasing early there only added waits, or spills.
+  static constexpr bool EARLY_RELEASE = QT == T_Q8_0 && NT == 1 && !DUAL;
   static constexpr int NF = 4 * NT * NMAT;               // accumulator floats per lane
   static constexpr int SLOT = 4 * 32 * NF * 4;           // one CTA's partial tile
 };
 
 template <int QT, int NT, bool DUAL>
-__global__ void __launch_bounds__(TC_THREADS, 2)
+__global__ void __launch_bounds__(TcShape<QT, NT, DUAL>::THREADS, 2)
 tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mS0,
           const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mS1,
           const __grid_constant__ CUtensorMap mX, const TcParams p) {
@@ -211,6 +241,10 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ns * S::STAGE);  // A, S, x landed
   uint64_t* empty = full + ns;                                                 // stage free
+  // Shared-memory addresses as 32-bit values; stage s starts at st0 + s * STAGE,
+  // its barriers at full0 + 8 s and empty0 + 8 s.
+  const uint32_t st0 = smem_u32(stages);
+  const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = blockIdx.x % p.ksplit;
@@ -221,17 +255,17 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   const int nu = u1 - u0;
 
   // Stage layout: [A, S (weights)] [x: 4 boxes of [CPAD][64] f16, 128-byte
-  // swizzle]. full[s]: the TMA bytes of the stage; empty[s]: the 8 consumers.
+  // swizzle]. full[s]: the TMA bytes of the stage; empty[s]: the consumers.
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], TC_CONSUMERS);
+      mbar_init(&empty[s], S::CONS);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  const bool producer = warp == TC_WARP_TMA;
+  const bool producer = warp == S::CONS;
   // Dependents may launch at once: another tensor-core GEMM queues its CTAs
   // behind this grid's and issues its first weight loads as soon as it lands.
   // The host never lets a CUDA-core kernel follow this one programmatically
@@ -241,25 +275,24 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   if (producer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
-      auto load_weights = [&](int s, int u) {
-        uint8_t* st = stages + (size_t)s * S::STAGE;
+      auto load_weights = [&](uint32_t st, uint32_t fb, int u) {
 #pragma unroll
         for (int m = 0; m < S::NMAT; ++m) {
           const CUtensorMap* mA = m == 0 ? &mA0 : &mA1;
           const CUtensorMap* mS = m == 0 ? &mS0 : &mS1;
-          uint8_t* a = st + m * S::A_BYTES;
+          const uint32_t a = st + m * S::A_BYTES;
 #pragma unroll
           for (int bx = 0; bx < S::QROW / 128; ++bx)
-            tma_load_2d(a + bx * TC_BM * 128, mA, u * S::QROW + bx * 128, m0, &full[s], pol_w);
-          tma_load_2d(st + S::NMAT * S::A_BYTES + m * S::S_BYTES, mS, u * 8, m0, &full[s], pol_w);
+            tma_load_2d(a + bx * TC_BM * 128, mA, u * S::QROW + bx * 128, m0, fb, pol_w);
+          tma_load_2d(st + S::NMAT * S::A_BYTES + m * S::S_BYTES, mS, u * 8, m0, fb, pol_w);
         }
       };
-      auto load_x = [&](int s, int u) {
+      auto load_x = [&](uint32_t st, uint32_t fb, int u) {
         // x[0..CPAD)[u*256 .. u*256+256) as [4][CPAD][64] (3-D map, see tc_launch)
         asm volatile(
             "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(stages + (size_t)s * S::STAGE + S::AS_BYTES)),
-            "l"(&mX), "r"(0), "r"(0), "r"(u * 4), "r"(smem_u32(&full[s]))
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(st + S::AS_BYTES),
+            "l"(&mX), "r"(0), "r"(0), "r"(u * 4), "r"(fb)
             : "memory");
       };
       // The weights of the first ring's worth of stages are requested before
@@ -267,23 +300,24 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       // their x follows the wait.
       const int npre = nu < ns ? nu : ns;
       for (int i = 0; i < npre; ++i) {
-        mbar_expect_tx(&full[i], (uint32_t)(S::AS_BYTES + S::X_BYTES));
-        load_weights(i, u0 + i);
+        mbar_expect_tx(full0 + 8 * i, (uint32_t)S::STAGE);
+        load_weights(st0 + i * S::STAGE, full0 + 8 * i, u0 + i);
       }
       pdl_wait();
-      for (int i = 0; i < npre; ++i) load_x(i, u0 + i);
+      for (int i = 0; i < npre; ++i) load_x(st0 + i * S::STAGE, full0 + 8 * i, u0 + i);
       // stage s and phase bit ph advance incrementally (no division in the loop)
       for (int i = npre, s = 0, ph = 1; i < nu; ++i, s = s + 1 == ns ? 0 : s + 1, ph ^= s == 0) {
-        if (!mbar_wait(&empty[s], (uint32_t)(ph ^ 1))) break;
-        mbar_expect_tx(&full[s], (uint32_t)(S::AS_BYTES + S::X_BYTES));
-        load_x(s, u0 + i);
-        load_weights(s, u0 + i);
+        if (!mbar_wait(empty0 + 8 * s, (uint32_t)(ph ^ 1))) break;
+        const uint32_t st = st0 + s * S::STAGE, fb = full0 + 8 * s;
+        mbar_expect_tx(fb, (uint32_t)S::STAGE);
+        load_x(st, fb, u0 + i);
+        load_weights(st, fb, u0 + i);
       }
     }
     __syncwarp();
   }
 
-  const int mi = warp & 3, kj = (warp >> 2) & 1;
+  const int mi = warp & 3, kj = warp >> 2;  // m-tile, k-group (the producer: kj == KG)
   const int g = lane >> 2, t = lane & 3;
   float acc[S::NMAT][NT][4];
 #pragma unroll
@@ -294,140 +328,187 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       for (int e = 0; e < 4; ++e) acc[m][n][e] = 0.f;
 
   if (!producer) {
-    // k-group kj owns the four contiguous blocks 4kj..4kj+3 of every unit.
+    // The OR pattern of the Q4_0 dequantisation, held in a register for the
+    // whole loop (an opaque move: the compiler neither folds it into an
+    // immediate, which would split each extraction in two, nor reloads it).
+    uint32_t M;
+    asm volatile("mov.b32 %0, 0x64006400;" : "=r"(M));
+    // k-group kj owns the BPW contiguous blocks BPW*kj .. BPW*kj + BPW - 1 of
+    // every unit (block b of the warp: unit block BPW*kj + b).
     // ldmatrix source of this lane: lanes 0-7 rows 0-7 and lanes 8-15 rows 8-15
     // of the m-tile at chunk c; lanes 16-31 the same rows at chunk c+1. The
     // swizzled byte offsets depend only on the lane and k-group: computed once.
+    constexpr int BPW = S::BPW;
     const int lrow = mi * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
     const int lchunk = lane >> 4;
-    uint32_t aoff[4];  // per block j of the k-group (Q4_0 uses j = 0 and 2)
+    constexpr int NL = QT == T_Q4_0 ? BPW / 2 : BPW;  // A ldmatrix.x4 per matrix and stage
+    uint32_t aoff[NL];  // Q4_0: blocks (2l, 2l+1) of the warp; Q8_0: block l (both halves)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int l = 0; l < NL; ++l) {
       int chunk, box;
-      if (QT == T_Q4_0) { chunk = 4 * kj + j + lchunk; box = 0; }   // pair (j, j+1) for j even
-      else { chunk = 2 * j + lchunk; box = kj; }                     // block 4kj + j in box kj
-      aoff[j] = (uint32_t)(box * TC_BM * 128 + lrow * 128 + ((chunk ^ (lrow & 7)) << 4));
+      if (QT == T_Q4_0) {  // 16 bytes per block and row: one 128-byte box
+        chunk = BPW * kj + 2 * l + lchunk;
+        box = 0;
+      } else {             // 32 bytes per block and row: blocks 4 bx .. 4 bx + 3 in box bx
+        const int b = BPW * kj + l;
+        chunk = 2 * (b & 3) + lchunk;
+        box = b >> 2;
+      }
+      aoff[l] = (uint32_t)(box * TC_BM * 128 + lrow * 128 + ((chunk ^ (lrow & 7)) << 4));
     }
-    const uint32_t soff_g = (uint32_t)((mi * 16 + g) * 16 + 8 * kj);
-    const uint32_t soff_g8 = (uint32_t)((mi * 16 + g + 8) * 16 + 8 * kj);
+    const uint32_t soff_g = (uint32_t)(S::NMAT * S::A_BYTES + (mi * 16 + g) * 16 + 2 * BPW * kj);
     // B fragments: ldmatrix.x4 of x rows (columns) n*8 + (lane & 7) at the k
-    // offsets 0, 8, 16, 24 of a block (matrix lane >> 3). Block 4kj + j of the
-    // unit lies in x box 2kj + (j >> 1) at 16-byte chunk 4(j & 1) + (lane >> 3),
-    // stored at chunk ^ row (the 128-byte swizzle; rows are 128 bytes).
+    // offsets 0, 8, 16, 24 of a block (matrix lane >> 3). Unit block b lies in
+    // x box b >> 1 at 16-byte chunk 4(b & 1) + (lane >> 3), stored at
+    // chunk ^ row (the 128-byte swizzle; rows are 128 bytes).
     const int lm = lane >> 3, lr = lane & 7;
-    const uint32_t boff = (uint32_t)(S::AS_BYTES + 2 * kj * S::CPAD * 128 + lr * 128);
-    const uint32_t xo0 = (uint32_t)((lm ^ lr) << 4), xo1 = (uint32_t)(((4 + lm) ^ lr) << 4);
-    for (int i = 0, s = 0, ph = 0; i < nu; ++i, s = s + 1 == ns ? 0 : s + 1, ph ^= s == 0) {
-      if (!mbar_wait(&full[s], (uint32_t)ph)) break;
-      const uint32_t st = smem_u32(stages + (size_t)s * S::STAGE);
-      const uint32_t sbase = st + S::NMAT * S::A_BYTES;
-      const uint32_t bbase = st + boff;
-      // the 4 f16 scales of rows g and g+8 for this k-group's blocks, per matrix
-      float dg[S::NMAT][4], dg8[S::NMAT][4];
+    const uint32_t boff = (uint32_t)(S::AS_BYTES + (BPW * kj >> 1) * S::CPAD * 128 + lr * 128);
+    const uint32_t xo0 = boff + (uint32_t)((lm ^ lr) << 4), xo1 = boff + (uint32_t)(((4 + lm) ^ lr) << 4);
+    uint32_t st = st0, fb = full0, eb = empty0;
+    for (int i = 0, s = 0, ph = 0; i < nu; ++i) {
+      if (!mbar_wait(fb, (uint32_t)ph)) break;
+      // the BPW f16 scales of rows g and g+8 for this k-group's blocks, per matrix
+      float dg[S::NMAT][BPW], dg8[S::NMAT][BPW];
 #pragma unroll
       for (int m = 0; m < S::NMAT; ++m) {
-        uint32_t a0, a1, b0, b1;
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a0), "=r"(a1) : "r"(sbase + m * S::S_BYTES + soff_g));
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(b0), "=r"(b1) : "r"(sbase + m * S::S_BYTES + soff_g8));
-        dg[m][0] = h2f((uint16_t)(a0 & 0xffffu)); dg[m][1] = h2f((uint16_t)(a0 >> 16));
-        dg[m][2] = h2f((uint16_t)(a1 & 0xffffu)); dg[m][3] = h2f((uint16_t)(a1 >> 16));
-        dg8[m][0] = h2f((uint16_t)(b0 & 0xffffu)); dg8[m][1] = h2f((uint16_t)(b0 >> 16));
-        dg8[m][2] = h2f((uint16_t)(b1 & 0xffffu)); dg8[m][3] = h2f((uint16_t)(b1 >> 16));
+        uint32_t a[2], b[2];
+        if (BPW == 4) {
+          lds64(st + soff_g + m * S::S_BYTES, a[0], a[1]);
+          lds64(st + soff_g + m * S::S_BYTES + 128, b[0], b[1]);  // row g + 8
+        } else {
+          a[0] = lds32(st + soff_g + m * S::S_BYTES);
+          b[0] = lds32(st + soff_g + m * S::S_BYTES + 128);
+        }
+#pragma unroll
+        for (int q = 0; q < BPW / 2; ++q) {
+          dg[m][2 * q] = lo_f32(a[q]); dg[m][2 * q + 1] = hi_f32(a[q]);
+          dg8[m][2 * q] = lo_f32(b[q]); dg8[m][2 * q + 1] = hi_f32(b[q]);
+        }
       }
       // All shared-memory reads of the stage are issued first: the raw quant
       // words of rows g and g+8 (Q4_0: one ldmatrix covers blocks j, j+1;
       // Q8_0: one covers both 16-element halves of block j) and the B
       // fragments of the four blocks.
-      constexpr int NL = QT == T_Q4_0 ? 2 : 4;
       uint32_t W[S::NMAT][NL][4];
 #pragma unroll
       for (int m = 0; m < S::NMAT; ++m)
 #pragma unroll
         for (int l = 0; l < NL; ++l)
-          ldsm_x4(st + m * S::A_BYTES + aoff[QT == T_Q4_0 ? 2 * l : l], W[m][l][0], W[m][l][1],
-                  W[m][l][2], W[m][l][3]);
-      uint4 bf[4][NT];
+          ldsm_x4(st + m * S::A_BYTES + aoff[l], W[m][l][0], W[m][l][1], W[m][l][2], W[m][l][3]);
+      uint4 bf[BPW][NT];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < BPW; ++j)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
-          ldsm_x4(bbase + (uint32_t)((j >> 1) * S::CPAD * 128 + n * 1024) + ((j & 1) ? xo1 : xo0),
+          ldsm_x4(st + ((j & 1) ? xo1 : xo0) + (uint32_t)((j >> 1) * S::CPAD * 128 + n * 1024),
                   bf[j][n].x, bf[j][n].y, bf[j][n].z, bf[j][n].w);
-      // Then the blocks in groups of JB, so that every group carries four
-      // independent mma chains whatever the tile shape.
-      constexpr int JB = 4 / (S::NMAT * NT) > 0 ? 4 / (S::NMAT * NT) : 1;
-#pragma unroll
-      for (int jb = 0; jb < 4; jb += JB) {
-        uint32_t A0[JB][S::NMAT][4], A1[JB][S::NMAT][4];
-#pragma unroll
-        for (int jj = 0; jj < JB; ++jj)
-#pragma unroll
-          for (int m = 0; m < S::NMAT; ++m) {
-            const int j = jb + jj;
-            if (QT == T_Q4_0) {
-              const uint32_t wg = W[m][j >> 1][(j & 1) ? 2 : 0];
-              const uint32_t wg8 = W[m][j >> 1][(j & 1) ? 3 : 1];
-              uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
-              dq4_f16(wg, e0, e1, e2, e3);
-              dq4_f16(wg8, f0, f1, f2, f3);
-              A0[jj][m][0] = e0; A0[jj][m][1] = f0; A0[jj][m][2] = e2; A0[jj][m][3] = f2;
-              A1[jj][m][0] = e1; A1[jj][m][1] = f1; A1[jj][m][2] = e3; A1[jj][m][3] = f3;
-            } else {
-              uint32_t p0, p1, q0, q1;
-              dq8_f16(W[m][j][0], p0, p1);
-              dq8_f16(W[m][j][1], q0, q1);
-              A0[jj][m][0] = p0; A0[jj][m][1] = q0; A0[jj][m][2] = p1; A0[jj][m][3] = q1;
-              dq8_f16(W[m][j][2], p0, p1);
-              dq8_f16(W[m][j][3], q0, q1);
-              A1[jj][m][0] = p0; A1[jj][m][1] = q0; A1[jj][m][2] = p1; A1[jj][m][3] = q1;
-            }
-          }
-        float fr[JB][S::NMAT][NT][4];
-#pragma unroll
-        for (int jj = 0; jj < JB; ++jj)
-#pragma unroll
-          for (int m = 0; m < S::NMAT; ++m)
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-              mma16816(fr[jj][m][n], A0[jj][m], bf[jb + jj][n].x, bf[jb + jj][n].y);
-#pragma unroll
-        for (int jj = 0; jj < JB; ++jj)
-#pragma unroll
-          for (int m = 0; m < S::NMAT; ++m)
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-              mma16816_acc(fr[jj][m][n], A1[jj][m], bf[jb + jj][n].z, bf[jb + jj][n].w);
-#pragma unroll
-        for (int jj = 0; jj < JB; ++jj)
-#pragma unroll
-          for (int m = 0; m < S::NMAT; ++m)
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-              const int j = jb + jj;
-              acc[m][n][0] = fmaf(dg[m][j], fr[jj][m][n][0], acc[m][n][0]);
-              acc[m][n][1] = fmaf(dg[m][j], fr[jj][m][n][1], acc[m][n][1]);
-              acc[m][n][2] = fmaf(dg8[m][j], fr[jj][m][n][2], acc[m][n][2]);
-              acc[m][n][3] = fmaf(dg8[m][j], fr[jj][m][n][3], acc[m][n][3]);
-            }
+      // Early release: the whole stage is now in registers. The proxy fence
+      // makes the release wait until this thread's shared-memory reads of the
+      // stage have completed (the stage is refilled by TMA, the async proxy,
+      // once every consumer has arrived).
+      auto release = [&]() {
+        __syncwarp();
+        mbar_arrive_lane0(eb, lane);
+        if (++s == ns) {  // next stage (ring of ns; the phase bit flips at the wrap)
+          s = 0;
+          ph ^= 1;
+          st = st0; fb = full0; eb = empty0;
+        } else {
+          st += S::STAGE; fb += 8; eb += 8;
+        }
+      };
+      if (S::EARLY_RELEASE) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        release();
       }
-      // The stage was read through the generic proxy (ldmatrix / ld.shared) and
-      // is refilled by TMA through the async proxy: order the reads before the
-      // release with a proxy fence, or the refill can overtake them.
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      // Then the blocks as a software pipeline: the tensor pipe takes a new
+      // mma only every few cycles, so block j's two dependent mma are issued
+      // around the dequantisation of block j + 1, and block j - 1's scale FMAs
+      // follow once its sums are out.
+      uint32_t A0[BPW][S::NMAT][4], A1[BPW][S::NMAT][4];
+      float fr[BPW][S::NMAT][NT][4];
+      auto dequant = [&](int j) {
+#pragma unroll
+        for (int m = 0; m < S::NMAT; ++m) {
+          if (QT == T_Q4_0) {
+            const uint32_t wg = W[m][j >> 1][(j & 1) ? 2 : 0];
+            const uint32_t wg8 = W[m][j >> 1][(j & 1) ? 3 : 1];
+            uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
+            dq4_f16(wg, M, e0, e1, e2, e3);
+            dq4_f16(wg8, M, f0, f1, f2, f3);
+            A0[j][m][0] = e0; A0[j][m][1] = f0; A0[j][m][2] = e2; A0[j][m][3] = f2;
+            A1[j][m][0] = e1; A1[j][m][1] = f1; A1[j][m][2] = e3; A1[j][m][3] = f3;
+          } else {
+            uint32_t p0, p1, q0, q1;
+            dq8_f16(W[m][j][0], p0, p1);
+            dq8_f16(W[m][j][1], q0, q1);
+            A0[j][m][0] = p0; A0[j][m][1] = q0; A0[j][m][2] = p1; A0[j][m][3] = q1;
+            dq8_f16(W[m][j][2], p0, p1);
+            dq8_f16(W[m][j][3], q0, q1);
+            A1[j][m][0] = p0; A1[j][m][1] = q0; A1[j][m][2] = p1; A1[j][m][3] = q1;
+          }
+        }
+      };
+      auto mma_lo = [&](int j) {
+#pragma unroll
+        for (int m = 0; m < S::NMAT; ++m)
+#pragma unroll
+          for (int n = 0; n < NT; ++n) mma16816(fr[j][m][n], A0[j][m], bf[j][n].x, bf[j][n].y);
+      };
+      auto mma_hi = [&](int j) {
+#pragma unroll
+        for (int m = 0; m < S::NMAT; ++m)
+#pragma unroll
+          for (int n = 0; n < NT; ++n) mma16816_acc(fr[j][m][n], A1[j][m], bf[j][n].z, bf[j][n].w);
+      };
+      auto scale = [&](int j) {
+#pragma unroll
+        for (int m = 0; m < S::NMAT; ++m)
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            acc[m][n][0] = fmaf(dg[m][j], fr[j][m][n][0], acc[m][n][0]);
+            acc[m][n][1] = fmaf(dg[m][j], fr[j][m][n][1], acc[m][n][1]);
+            acc[m][n][2] = fmaf(dg8[m][j], fr[j][m][n][2], acc[m][n][2]);
+            acc[m][n][3] = fmaf(dg8[m][j], fr[j][m][n][3], acc[m][n][3]);
+          }
+      };
+      dequant(0);
+#pragma unroll
+      for (int j = 0; j < BPW; ++j) {
+        mma_lo(j);
+        if (j + 1 < BPW) dequant(j + 1);
+        mma_hi(j);
+        if (j > 0) scale(j - 1);
+      }
+      scale(BPW - 1);
+      if (!S::EARLY_RELEASE) {
+        // Release after the arithmetic. Every value read from the stage (quant
+        // words and x through ldmatrix, scales through ld.shared) feeds an
+        // instruction that issues before the arrive (the mma consume the words
+        // and x; the scale FMAs, pinned here by the empty asm that takes the
+        // accumulators, consume the scales), and an instruction issues only
+        // once its operands have arrived: no read of the stage is outstanding
+        // when the producer may refill it.
+#pragma unroll
+        for (int m = 0; m < S::NMAT; ++m)
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+            asm volatile("" ::"f"(acc[m][n][0]), "f"(acc[m][n][1]), "f"(acc[m][n][2]),
+                         "f"(acc[m][n][3]));
+        release();
+      }
     }
   }
 
   // y0, y and h are read or written only after every earlier kernel on the
   // stream has finished
   pdl_wait();
-  // ---- reduce the two k-groups (fixed order: kj 0 + kj 1) in shared memory
+  // ---- reduce the k-groups in shared memory (fixed order: kj 0 + kj 1 + ...)
   float* scratch = reinterpret_cast<float*>(stages);
   if (!producer) {
-    asm volatile("bar.sync 1, %0;" ::"n"(TC_CONSUMERS * 32) : "memory");
-    if (kj == 1) {
-      float* dst = scratch + (size_t)(mi * 32 + lane) * S::NF;
+    asm volatile("bar.sync 1, %0;" ::"n"(S::CONS * 32) : "memory");
+    if (kj > 0) {
+      float* dst = scratch + (size_t)((kj - 1) * 4 * 32 + mi * 32 + lane) * S::NF;
       int q = 0;
 #pragma unroll
       for (int m = 0; m < S::NMAT; ++m)
@@ -436,16 +517,19 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[q++] = acc[m][n][e];
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(TC_CONSUMERS * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(S::CONS * 32) : "memory");
     if (kj == 0) {
-      const float* srcp = scratch + (size_t)(mi * 32 + lane) * S::NF;
-      int q = 0;
 #pragma unroll
-      for (int m = 0; m < S::NMAT; ++m)
+      for (int r = 1; r < S::KG; ++r) {
+        const float* srcp = scratch + (size_t)((r - 1) * 4 * 32 + mi * 32 + lane) * S::NF;
+        int q = 0;
 #pragma unroll
-        for (int n = 0; n < NT; ++n)
+        for (int m = 0; m < S::NMAT; ++m)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[m][n][e] += srcp[q++];
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[m][n][e] += srcp[q++];
+      }
     }
   }
 
@@ -566,8 +650,8 @@ TcConfig pick_config_budget(int rows, int k, size_t budget, const int (&cap)[9])
     if (ns > nu_max) ns = nu_max;
     if (ns < 2 && nu_max >= 2) continue;
     if (ns < 1) continue;
-    const size_t reuse = (size_t)ns * S::STAGE;
-    if ((size_t)S::SLOT > reuse || (size_t)(ks - 1) * S::SLOT > reuse) continue;
+    const size_t reuse = (size_t)ns * S::STAGE;  // k-group and cluster partials reuse the ring
+    if ((size_t)(S::KG - 1) * S::SLOT > reuse || (size_t)(ks - 1) * S::SLOT > reuse) continue;
     return TcConfig{ks, ns, 1024 + reuse + 2 * ns * sizeof(uint64_t)};
   }
   return TcConfig{0, 0, 0};
@@ -640,7 +724,7 @@ cudaError_t tc_launch(const void* q, const uint16_t* scl, const void* qu, const 
   if (e != cudaSuccess) return e;
   const int ntile = (rows + TC_BM - 1) / TC_BM;
   (void)S::NF;
-  return launch_pdl(kern, dim3((unsigned)(ntile * cfg.ksplit)), dim3(TC_THREADS), cfg.smem, s,
+  return launch_pdl(kern, dim3((unsigned)(ntile * cfg.ksplit)), dim3(S::THREADS), cfg.smem, s,
                     cfg.ksplit, LC_SMEM, mA0, mS0, mA1, mS1, mX, p);
 }
 
