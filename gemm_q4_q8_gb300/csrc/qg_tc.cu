@@ -119,6 +119,12 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
+                                       uint32_t& d) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr));
+}
 __device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
 }
@@ -200,13 +206,17 @@ struct TcParams {
 
 // KG k-groups of consumer warps split a unit's 8 blocks (8 / KG blocks per warp
 // and unit); 4 m-tiles x KG k-groups of consumers plus one TMA producer warp.
-// (4 k-groups, 16 consumer warps with half the work each, measured slower:
-// every warp pays the per-stage waits and address work, and the instruction
-// count per weight rose by half. Two units per stage behind one pair of
-// barriers measured no faster.)
+// The single-matrix 1-8-column plan uses one k-group: four consumer warps, each
+// with one m-tile across the whole unit (fewer per-stage waits and address
+// work per weight, eight independent blocks per warp; small matrices ran 5%
+// faster). The 16-column and fused plans keep two k-groups: one k-group
+// measured no faster there and spilled in the fused plan. (Four k-groups, 16
+// consumer warps with half the work each, measured slower: every warp pays the
+// per-stage overhead. Two units per stage behind one pair of barriers measured
+// no faster.)
 template <int QT, int NT, bool DUAL>
 struct TcShape {
-  static constexpr int KG = 2;
+  static constexpr int KG = (NT == 1 && !DUAL) ? 1 : 2;
   static constexpr int BPW = 8 / KG;                     // blocks per warp and unit
   static constexpr int CONS = 4 * KG;                    // consumer warps
   static constexpr int THREADS = (CONS + 1) * 32;        // + the producer warp (last)
@@ -319,6 +329,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 
   const int mi = warp & 3, kj = warp >> 2;  // m-tile, k-group (the producer: kj == KG)
   const int g = lane >> 2, t = lane & 3;
+  float y0v[NT][4];  // the epilogue's residual (rank 0, k-group 0; loaded in the loop)
   float acc[S::NMAT][NT][4];
 #pragma unroll
   for (int m = 0; m < S::NMAT; ++m)
@@ -367,12 +378,30 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     uint32_t st = st0, fb = full0, eb = empty0;
     for (int i = 0, s = 0, ph = 0; i < nu; ++i) {
       if (!mbar_wait(fb, (uint32_t)ph)) break;
+      if (i == 0 && !DUAL && p.y0 && kj == 0 && rank == 0) {
+        // The epilogue's residual, fetched now rather than after the loop (its
+        // DRAM round trip then overlaps the stream). It comes from an earlier
+        // kernel on the stream: wait for that kernel first (the first stage's x
+        // implies it has completed; the wait makes its writes visible here).
+        pdl_wait();
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = m0 + mi * 16 + g + ((e >> 1) << 3);
+            const int col = n * 8 + 2 * t + (e & 1);
+            y0v[n][e] = (row < p.rows && col < p.ncols) ? p.y0[(size_t)col * p.rows + row] : 0.f;
+          }
+      }
       // the BPW f16 scales of rows g and g+8 for this k-group's blocks, per matrix
       float dg[S::NMAT][BPW], dg8[S::NMAT][BPW];
 #pragma unroll
       for (int m = 0; m < S::NMAT; ++m) {
-        uint32_t a[2], b[2];
-        if (BPW == 4) {
+        uint32_t a[4], b[4];
+        if (BPW == 8) {
+          lds128(st + soff_g + m * S::S_BYTES, a[0], a[1], a[2], a[3]);
+          lds128(st + soff_g + m * S::S_BYTES + 128, b[0], b[1], b[2], b[3]);  // row g + 8
+        } else if (BPW == 4) {
           lds64(st + soff_g + m * S::S_BYTES, a[0], a[1]);
           lds64(st + soff_g + m * S::S_BYTES + 128, b[0], b[1]);  // row g + 8
         } else {
@@ -582,7 +611,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         p.h[o] = __float2half_rn(silu_f32(acc[0][n][e]) * acc[S::NMAT - 1][n][e]);
       } else {
         float v = acc[0][n][e];
-        if (p.y0) v += p.y0[o];
+        if (p.y0) v += nu > 0 ? y0v[n][e] : p.y0[o];
         p.y[o] = v;
       }
     }
