@@ -81,6 +81,28 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
             assert_within(y_na, oracle.moe(case)[0], bound, f"noalloc call {call} vs oracle")
 
 
+@pytest.mark.gpu
+def test_noalloc_at_its_largest_accepted_workspace():
+    """16 columns x top-15 with ffn 2048 needs exactly the whole library array
+    (1 MiB of h). Two calls in a row, each bit for bit equal to the workspace
+    call (a 24-expert stack keeps the test small; the workspace does not depend
+    on the number of experts)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gemm_q4_q8_gb300 import build
+    build.build()
+    case = synth.moe_case(synth.Q4_0, 24, 2048, 2048, 16, topk=15, shared=True, residual=True,
+                          seed=13)
+    assert qg.qmoe_workspace_bytes(24, 2048, 2048, 16, 15) == qg.QG_MOE_NOALLOC_WS_BYTES
+    a = _moe_args(case)
+    y_ws, u_ws, e_ws = _run(case, a, noalloc=False)
+    assert np.isfinite(y_ws).all()
+    for call in (1, 2):
+        y_na, u_na, e_na = _run(case, a, noalloc=True)
+        assert np.array_equal(y_na.view(np.uint32), y_ws.view(np.uint32)), call
+        assert np.array_equal(u_na, u_ws) and e_na == e_ws == 0
+
+
 def test_noalloc_workspace_holds_every_accepted_shape():
     """The library's array is as large as the largest workspace any accepted
     shape needs; shapes the MoE layer rejects get the same status from both
