@@ -270,39 +270,42 @@ class GpuStep:
 
     def step_e2e(self, stream, i: int):
         """Step i end to end: its inputs go up from pinned host memory, the six
-        calls run, its outputs come down to pinned host memory. Copies run on a
-        copy stream with device buffer set i % 2, so step i+1's upload and step
-        i's download overlap the kernels of the neighbouring step; events keep
-        every buffer's writes and reads in order."""
+        calls run, its outputs come down to pinned host memory. Uploads and
+        downloads run on two copy streams of their own (one in-order copy
+        stream would queue step i+1's upload behind step i's download, and so
+        behind step i's kernels), with device buffer set i % 2, so step i+1's
+        upload and step i's download overlap the kernels of the neighbouring
+        step; events keep every buffer's writes and reads in order."""
         t = self.torch
         if self.copy_stream is None:
-            self.copy_stream = t.cuda.Stream()
+            self.copy_stream = (t.cuda.Stream(), t.cuda.Stream())  # uploads, downloads
             self.ev = {k: [t.cuda.Event(), t.cuda.Event()] for k in ("up", "run", "down")}
             self.used = [False, False]
-        cs, b = self.copy_stream, i % 2
+        (us, ds), b = self.copy_stream, i % 2
         ev = self.ev
-        with t.cuda.stream(cs):
+        with t.cuda.stream(us):
             if i == 0:
-                cs.wait_stream(stream)           # the timed region starts before the first upload
+                us.wait_stream(stream)           # the timed region starts before the first upload
             if self.used[b]:
-                cs.wait_event(ev["run"][b])      # step i-2 has finished reading set b
+                us.wait_event(ev["run"][b])      # step i-2 has finished reading set b
             self.din_flat[b].copy_(self.pin_in_flat, non_blocking=True)
-            ev["up"][b].record(cs)
+            ev["up"][b].record(us)
         stream.wait_event(ev["up"][b])
         if self.used[b]:
             stream.wait_event(ev["down"][b])     # step i-2's outputs have left set b
         self.step(stream, buf=b)
         ev["run"][b].record(stream)
-        with t.cuda.stream(cs):
-            cs.wait_event(ev["run"][b])
+        with t.cuda.stream(ds):
+            ds.wait_event(ev["run"][b])
             self.pin_out_flat.copy_(self.dout_flat[b], non_blocking=True)
-            ev["down"][b].record(cs)
+            ev["down"][b].record(ds)
         self.used[b] = True
 
     def e2e_join(self, stream):
         """Make `stream` wait for every copy issued so far."""
         if self.copy_stream is not None:
-            stream.wait_stream(self.copy_stream)
+            for cs in self.copy_stream:
+                stream.wait_stream(cs)
 
     def e2e_bytes(self):
         """Bytes of the one upload and the one download of a step (the flat

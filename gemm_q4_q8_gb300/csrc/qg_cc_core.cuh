@@ -5,17 +5,25 @@
 
 namespace qg {
 
-// One block's quants for one row.
+// One block's quants for one row. load: from global memory (streamed, read
+// once); load_shared: from a copy in shared memory (16-byte aligned).
 template <int QT> struct Blk;
 template <> struct Blk<T_Q4_0> {
   uint4 a;
   __device__ __forceinline__ void load(const uint8_t* p) { a = ld_stream16(p); }
+  __device__ __forceinline__ void load_shared(const uint8_t* p) {
+    a = *reinterpret_cast<const uint4*>(p);
+  }
 };
 template <> struct Blk<T_Q8_0> {
   uint4 a, b;
   __device__ __forceinline__ void load(const uint8_t* p) {
     a = ld_stream16(p);
     b = ld_stream16(p + 16);
+  }
+  __device__ __forceinline__ void load_shared(const uint8_t* p) {
+    a = reinterpret_cast<const uint4*>(p)[0];
+    b = reinterpret_cast<const uint4*>(p)[1];
   }
 };
 

@@ -155,12 +155,17 @@ __device__ __forceinline__ Q8Word dequant_q8_word(uint32_t w) {
 // Kernels of this library are launched with programmatic stream
 // serialisation: a kernel may start while the previous kernel on the stream is
 // finishing. pdl_trigger() lets the next kernel start early (every kernel
-// calls it at its start; the host keeps a CUDA-core kernel from starting early
-// behind the tensor-core kernel, see LaunchClass in qg_internal.h); pdl_wait() blocks
+// calls it at its start, except the MoE gate/up kernel, which calls it right
+// after its wait; the host keeps a CUDA-core kernel from starting early behind
+// the tensor-core kernel, see LaunchClass in qg_internal.h); pdl_wait() blocks
 // until every earlier kernel on the stream has completed and its writes are
 // visible. Each kernel reads only weights (immutable inputs) before pdl_wait()
-// and touches activations, residuals, ids and outputs only after it. Launched
-// without the attribute, both instructions are no-ops.
+// and touches activations, residuals, ids and outputs only after it, with one
+// exception: the staged MoE down kernel reads the id list and the routing
+// weights before its wait. It is launched behind the gate/up kernel, which lets
+// it start only once its own wait has returned, so whatever wrote them has
+// completed by then. Launched without the attribute, both instructions are
+// no-ops.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

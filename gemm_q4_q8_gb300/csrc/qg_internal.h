@@ -121,6 +121,8 @@ bool moe_shape_supported(int ffn, int hidden, int ncols, int topk);
 // Type and shape checks of the MoE layer: QG_OK, QG_ERR_TYPE or QG_ERR_SHAPE.
 qg_status moe_check_shape(int t, int n_expert, int ffn, int hidden, int ncols, int topk);
 cudaError_t moe_forward(const MoeArgs& a, cudaStream_t s);
+// The MoE kernels' device error word (QG_DEV_ERR_WAIT), read and cleared.
+cudaError_t moe_device_error(int32_t* bits);
 
 cudaError_t repack_launch(int qt, const void* gguf, int rows, int k, void* q_out,
                           uint16_t* scl_out, cudaStream_t s);

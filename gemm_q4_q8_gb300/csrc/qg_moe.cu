@@ -24,10 +24,16 @@
 //                 fixed butterfly sums the lanes of a row, and
 //                 y = y0 + total is written once. The summation order depends
 //                 only on the shape, so results are identical run to run.
+//                 Two kernels compute it with the same arithmetic: for one or
+//                 two columns the CTA's row slices of all its down matrices
+//                 are staged in shared memory by bulk copies issued before the
+//                 kernel waits on K1; otherwise each lane streams its blocks
+//                 through registers.
 // An id outside [0, E) contributes nothing and sets a bit in the caller's error
 // word; no trap is raised and no CTA waits on another.
 #include <cuda_runtime.h>
 
+#include "qg_async.cuh"
 #include "qg_cc_core.cuh"
 #include "qg_internal.h"
 
@@ -125,20 +131,27 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) moe_gate_up_ke
   constexpr int QB = QTraits<QT>::QB;
   const int n = p.ncols * p.topk;
   const int t = threadIdx.x;
-  pdl_trigger();
+  const int k = p.hidden;
+  // Dependents may launch only once this kernel has passed its wait: the
+  // staged down kernel reads ids and rw before its own wait, and by then the
+  // kernel that wrote them has completed.
   pdl_wait();  // ids and x come from earlier kernels on the stream
+  pdl_trigger();
+
+  // The ids are loaded first; x is staged while they are in flight.
+  int id = -1;
+  if (t < n) id = p.ids[t];
+  stage_x_cols(QT, xs, k, p.x, (size_t)k, p.ncols, k);
 
   // Pair order: valid positions by (expert id, position), then the shared
   // expert's columns (codes n + c).
-  int id = -1;
   bool valid = false;
   if (t < n) {
-    id = p.ids[t];
     valid = id >= 0 && id < p.n_expert;
     s_ids[t] = valid ? id : -1;
   }
   if (t < MOE_MAXN) s_key[t] = valid ? id * MOE_MAXN + t : 0x7fffffff;
-  const int nvalid = __syncthreads_count(valid);
+  const int nvalid = __syncthreads_count(valid);  // also publishes the staged x
   if (valid) {
     // rank = number of keys below this one (keys are distinct)
     const int key = id * MOE_MAXN + t;
@@ -181,7 +194,6 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) moe_gate_up_ke
     if (t == 0 && nvalid < n && p.err_flag) atomicOr(p.err_flag, (int32_t)QG_MOE_BAD_ID);
   }
 
-  const int k = p.hidden;
   const int lane = t & 31, warp = t >> 5;
   const int nb = k / QK;
   const size_t rowbytes = (size_t)nb * QB;
@@ -191,9 +203,6 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) moe_gate_up_ke
   const int total = P * ngroups;
   const int stride = gridDim.x * WARPS;
   int item = blockIdx.x * WARPS + warp;
-
-  stage_x_cols(QT, xs, k, p.x, (size_t)k, p.ncols, k);
-  __syncthreads();
 
   for (; item < total; item += stride) {
     const MoeK1Rows<QT> cur = moe_k1_rows<QT>(p, s_order, s_ids, s_pc, s_pj, n, item / ngroups,
@@ -325,6 +334,142 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_down_kernel(const MoeDev p
   }
 }
 
+// ------------------------------------------- K2s: down + combine, staged
+// The arithmetic of moe_down_kernel (each lane sums its blocks in ascending
+// order, within a block the live experts in k order, then the same fixed
+// butterfly per row), so the two kernels give bit-identical outputs. A CTA owns
+// one column and R consecutive output rows; one thread brings the R-row slices
+// of all the column's down matrices into shared memory with bulk copies issued
+// before the kernel waits on its predecessor, so the down weights stream while
+// the gate/up kernel finishes. Reading ids and rw before that wait is safe:
+// the gate/up kernel lets its dependents launch only after its own wait, by
+// which time the kernel that wrote them has completed.
+//
+// Dynamic shared memory: h of the live entries as f32 planes [nj][ffn], then
+// per entry its R rows of quants [R][ffn/32 * QB] and of scales
+// [R][ffn/32] (padded to 16 bytes).
+__device__ int32_t g_moe_error = 0;  // QG_DEV_ERR_WAIT: a wait timed out
+
+template <int QT>
+__global__ void __launch_bounds__(MOE_THREADS, 2) moe_down_staged_kernel(const MoeDev p, int R) {
+  __shared__ int s_e[MOE_MAXJ];     // expert of each live entry (n_expert = shared)
+  __shared__ int s_j[MOE_MAXJ];     // its position j (h index)
+  __shared__ float s_w[MOE_MAXJ];   // its routing weight
+  __shared__ int s_nj;
+  __shared__ __align__(8) uint64_t s_bar;
+  extern __shared__ float4 smem_f4[];
+  constexpr int QB = QTraits<QT>::QB;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int k = p.ffn, nb = k / QK;
+  const int njmax = p.topk + (p.has_shared ? 1 : 0);
+  const uint32_t rowbytes = (uint32_t)nb * QB;
+  const uint32_t sstride = (uint32_t)((R * nb * 2 + 15) & ~15);
+  float* hs = reinterpret_cast<float*>(smem_f4);
+  uint8_t* wq = reinterpret_cast<uint8_t*>(hs + (size_t)njmax * k);
+  uint8_t* wsc = wq + (size_t)njmax * R * rowbytes;
+  pdl_trigger();
+  const int c = blockIdx.x % p.ncols, part = blockIdx.x / p.ncols;
+  const int r0 = part * R;
+  const int nrows = min(R, p.hidden - r0);  // a multiple of 8 (hidden % 32 == 0, R % 8 == 0)
+  if (warp == 0) {
+    // live entries of column c in k order (one load per lane, then a ballot)
+    int id = -1;
+    float w = 0.f;
+    if (lane < p.topk) {
+      id = p.ids[c * p.topk + lane];
+      w = p.rw[c * p.topk + lane];
+    }
+    const bool live = lane < p.topk && id >= 0 && id < p.n_expert;
+    const unsigned m = __ballot_sync(0xffffffffu, live);
+    if (live) {
+      const int at = __popc(m & ((1u << lane) - 1u));
+      s_e[at] = id; s_j[at] = lane; s_w[at] = w;
+    }
+    const int nl = __popc(m);
+    if (lane == 0) {
+      if (p.has_shared) { s_e[nl] = p.n_expert; s_j[nl] = p.topk; s_w[nl] = 1.f; }
+      s_nj = nl + (p.has_shared ? 1 : 0);
+      mbar_init(&s_bar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+  }
+  __syncthreads();
+  const int nj = s_nj;
+  const uint32_t bar = smem_u32(&s_bar);
+  if (t == 0) {
+    const size_t mat_q = (size_t)p.hidden * rowbytes;
+    const size_t mat_s = (size_t)p.hidden * nb;
+    mbar_expect_tx(bar, (uint32_t)nj * (uint32_t)nrows * (rowbytes + 2u * nb));
+    for (int m = 0; m < nj; ++m) {
+      const int e = s_e[m];
+      const uint8_t* qe = e == p.n_expert ? p.sqd : p.qd + (size_t)e * mat_q;
+      const uint16_t* se = e == p.n_expert ? p.ssd : p.sd + (size_t)e * mat_s;
+      bulk_g2s(smem_u32(wq + (size_t)m * R * rowbytes), qe + (size_t)r0 * rowbytes,
+               (uint32_t)nrows * rowbytes, bar);
+      bulk_g2s(smem_u32(wsc + (size_t)m * sstride), se + (size_t)r0 * nb,
+               (uint32_t)nrows * nb * 2u, bar);
+    }
+  }
+  pdl_wait();  // the gate/up results, and y0, come from earlier kernels
+  for (int it = t; it < nj * nb; it += blockDim.x) {
+    const int m = it / nb, b = it % nb;
+    stage_block(QT, hs + m * k, nb, b,
+                p.hws + ((size_t)c * (p.topk + 1) + s_j[m]) * k + (size_t)b * QK);
+  }
+  __syncthreads();
+  mbar_wait(bar, 0, &g_moe_error);
+
+  int lpr = 32;  // lanes per row: a power of two, at most the blocks of a row
+  while (lpr > nb) lpr >>= 1;
+  const int rpw = 32 / lpr;
+  const int rs = lane / lpr, bl = lane % lpr;
+  const int nitems = (R + rpw - 1) / rpw;
+  for (int item = warp; item < nitems; item += MOE_WARPS) {
+    // rows past the CTA's slice (when R is not a multiple of rpw) are computed
+    // on its last row and not stored
+    const int row = r0 + item * rpw + rs;
+    const int lr = min(row - r0, nrows - 1);
+    float acc = 0.f;
+    for (int b = bl; b < nb; b += lpr) {
+      for (int m = 0; m < nj; ++m) {
+        const uint8_t* qp = wq + ((size_t)m * R + lr) * rowbytes + (size_t)b * QB;
+        Blk<QT> q;
+        q.load_shared(qp);
+        const uint16_t sc =
+            *reinterpret_cast<const uint16_t*>(wsc + (size_t)m * sstride + ((size_t)lr * nb + b) * 2);
+        float2 xr[16];
+        load_x16(hs + m * k, nb, b, xr);
+        acc = fmaf(s_w[m] * h2f(sc), blk_dot(q, xr), acc);
+      }
+    }
+    for (int off = lpr >> 1; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (bl == 0 && row < r0 + nrows) {
+      const size_t o = (size_t)c * p.hidden + row;
+      p.y[o] = (p.y0 ? p.y0[o] : 0.f) + acc;
+    }
+  }
+}
+
+// Rows per CTA of the staged down kernel for this call, or 0 when the register
+// kernel runs instead: for more than two columns (measured at 256 experts,
+// ffn 512, hidden 2048, top-8 + shared: 1 column 14.3 -> 12.1 us per layer
+// call with the staged kernel, but 8 columns 47.8 -> 56.6 and 16 columns
+// 85.1 -> 103.0: its 1,024-2,048 short CTAs each stage h and wait out one
+// copy latency), or when its shared memory does not fit two CTAs per SM.
+static int moe_staged_rows(int qt, int ffn, int hidden, int ncols, int topk, int has_shared,
+                           size_t* smem) {
+  constexpr int R = 8;  // rows per CTA: 256 CTAs per column at hidden 2048
+  if (ncols > 2 || hidden < R) return 0;
+  const int nb = ffn / QK;
+  const size_t rowbytes = (size_t)nb * (qt == T_Q4_0 ? 16 : 32);
+  const int njmax = topk + (has_shared ? 1 : 0);
+  const size_t sstride = ((size_t)R * nb * 2 + 15) & ~(size_t)15;
+  const size_t need = (size_t)njmax * ((size_t)ffn * 4 + R * rowbytes + sstride);
+  if (need > 100 * 1024) return 0;
+  *smem = need;
+  return R;
+}
+
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 size_t moe_ws_bytes(int n_expert, int ffn, int hidden, int ncols, int topk) {
@@ -364,12 +509,31 @@ static cudaError_t moe_launch_t(const MoeDev& d, cudaStream_t s) {
     e = launch_moe(moe_gate_up_kernel<QT, 16>, 512, (pairs_max * ngroups + 15) / 16, 1, smem_gu, d, s);
   }
   if (e != cudaSuccess) return e;
+  size_t smem_ds = 0;
+  const int R = moe_staged_rows(QT, d.ffn, d.hidden, d.ncols, d.topk, d.has_shared, &smem_ds);
+  if (R > 0) {
+    auto kern = moe_down_staged_kernel<QT>;
+    if ((e = prepare_kernel(reinterpret_cast<const void*>(kern), smem_ds, false)) != cudaSuccess)
+      return e;
+    const int parts = (d.hidden + R - 1) / R;
+    // Launched as LC_L1, so the next kernel on the stream may still overlap its
+    // tail (measured 12.1 us per layer call at 1 column, 12.7 as LC_SMEM).
+    return launch_pdl(kern, dim3((unsigned)(parts * d.ncols)), dim3(MOE_THREADS), smem_ds, s, 0,
+                      LC_L1, d, R);
+  }
   const size_t smem_dn = (size_t)(d.topk + 1) * d.ffn * sizeof(float);
   const long big = 1L << 30;
   // one row per lane per item when few columns share the grid (more items,
   // all of a lane's experts in flight at once); two rows otherwise
   if (d.ncols <= 2) return launch_moe(moe_down_kernel<QT, 1, 9>, MOE_THREADS, big, d.ncols, smem_dn, d, s);
   return launch_moe(moe_down_kernel<QT, 2, 3>, MOE_THREADS, big, d.ncols, smem_dn, d, s);
+}
+
+cudaError_t moe_device_error(int32_t* bits) {
+  const int32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_moe_error, sizeof(*bits));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_moe_error, &zero, sizeof(zero));
+  return e;
 }
 
 cudaError_t moe_forward(const MoeArgs& a, cudaStream_t s) {

@@ -34,6 +34,7 @@
 
 #include <mutex>
 
+#include "qg_async.cuh"
 #include "qg_common.cuh"
 #include "qg_internal.h"
 
@@ -42,58 +43,12 @@ namespace qg {
 constexpr int TC_BM = 64;                 // rows per CTA
 constexpr int TC_KT = 256;                // weights per stage (one K unit)
 constexpr int TC_SMEM_BUDGET = 112 * 1024;  // two CTAs per SM
-constexpr long long TC_WAIT_LIMIT = 4000000000LL;  // cycles (~2 s) before giving up
-constexpr uint32_t TC_SUSPEND_NS = 1000000;        // suspend-time hint of one try_wait (1 ms)
 
 __device__ int32_t g_tc_error = 0;        // QG_DEV_ERR_WAIT: a wait timed out
 
 // ------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-// Arrive once per warp, from lane 0, without a divergent branch.
-__device__ __forceinline__ void mbar_arrive_lane0(uint32_t bar, int lane) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %1, 0;\n\t"
-      "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar), "r"(lane)
-      : "memory");
-}
-// One try_wait on a phase: the warp may be parked until the phase completes
-// (or the hint runs out), so a wait on a stage that is not ready yet costs no
-// polling loop.
-__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(TC_SUSPEND_NS)
-      : "memory");
-  return ok;
-}
-// The rest of a wait whose first try failed: bounded by the clock (~2 s), after
-// which the error bit is set and the caller falls through.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > TC_WAIT_LIMIT) {
-      atomicOr(&g_tc_error, QG_DEV_ERR_WAIT);
-      return false;
-    }
-  }
-  return true;
-}
-// Bounded wait on a phase of an mbarrier; false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity);
+  return mbar_wait(bar, parity, &g_tc_error);
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar, uint64_t policy) {
@@ -805,6 +760,8 @@ extern "C" qg_status qg_device_error(int32_t* bits_out) {
   const int32_t zero = 0;
   if (cudaMemcpyFromSymbol(&v, qg::g_tc_error, sizeof(v)) != cudaSuccess) return QG_ERR_CUDA;
   if (cudaMemcpyToSymbol(qg::g_tc_error, &zero, sizeof(zero)) != cudaSuccess) return QG_ERR_CUDA;
-  *bits_out = v;
+  int32_t m = 0;
+  if (qg::moe_device_error(&m) != cudaSuccess) return QG_ERR_CUDA;
+  *bits_out = v | m;
   return QG_OK;
 }

@@ -153,6 +153,29 @@ def test_moe_16_columns_top16():
     assert nu == len(np.unique(case["ids"]))
 
 
+def test_moe_two_columns_no_shared():
+    """Two columns (the down projection stages its row slices in shared memory
+    by bulk copies), Q4_0, no shared expert, a residual, a duplicate and an
+    out-of-range id."""
+    case = synth.moe_case(synth.Q4_0, 24, 256, 384, 2, topk=6, shared=False, residual=True,
+                          seed=12)
+    ids = case["ids"].copy()
+    ids[0, 3] = ids[0, 1]
+    ids[1, 5] = 24
+    check_moe(case, ids=ids, what="MoE Q4_0, 2 columns, no shared expert")
+
+
+@pytest.mark.parametrize("ncols", [1, 3])
+def test_moe_wide_ffn(ncols):
+    """ffn 1024 with top-8 and a shared expert: the down projection's row slices
+    of all nine experts do not fit in shared memory beside h, so the down and
+    combine run on the kernel that streams them through registers (at ffn 512
+    they are staged in shared memory by bulk copies)."""
+    case = synth.moe_case(synth.Q8_0, 12, 1024, 256, ncols, topk=8, shared=True, residual=True,
+                          seed=7 + ncols)
+    check_moe(case, what=f"MoE ffn 1024, top-8 + shared, C={ncols}")
+
+
 def test_moe_topk_one_and_all_experts_shared():
     case = synth.moe_case(synth.Q8_0, 3, 64, 64, 8, topk=1, shared=True, residual=False, seed=5)
     check_moe(case, what="MoE topk=1, 3 experts, 8 columns")
