@@ -62,6 +62,34 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err) {
   return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, err);
 }
+// As mbar_wait, with acquire semantics at cluster scope: the writes that other
+// CTAs of the cluster made before their release arrivals on this barrier are
+// visible once the phase has completed.
+__device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ASYNC_SUSPEND_NS)
+      : "memory");
+  return ok;
+}
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity,
+                                                           int32_t* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (clock64() - t0 > ASYNC_WAIT_LIMIT) {
+      atomicOr(err, QG_DEV_ERR_WAIT);
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int32_t* err) {
+  return mbar_try_wait_cluster(bar, parity) || mbar_wait_cluster_slow(bar, parity, err);
+}
 // Bulk copy of `bytes` contiguous bytes from global to this CTA's shared
 // memory, completing on the mbarrier `bar` (its transaction count must have
 // been raised by the bytes first). Both addresses 16-byte aligned, bytes a

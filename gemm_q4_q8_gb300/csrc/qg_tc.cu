@@ -23,9 +23,11 @@
 //    product is scaled by its f16 scale in f32, so the only roundings are the
 //    f32 accumulations.
 //  * The two k-groups are summed in a fixed order through shared memory, then
-//    the cluster's CTAs are summed in rank order through distributed shared
-//    memory by the rank-0 CTA, which runs the epilogue (y = y0 + acc, or
-//    h = f16(SiLU(g) * u)). The reduction tree depends only on the shape.
+//    the cluster's CTAs are summed in rank order by the rank-0 CTA: the other
+//    ranks store their partial tiles into its shared memory and arrive on one
+//    of its mbarriers (no cluster-wide barrier after the stream), and rank 0
+//    runs the epilogue (y = y0 + acc, or h = f16(SiLU(g) * u)). The reduction
+//    tree depends only on the shape.
 // Every wait is bounded: on timeout the kernel records an error bit in a device
 // word and falls through instead of spinning forever.
 #include <cuda.h>
@@ -204,8 +206,12 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
                                              ~(uintptr_t)1023);
   const int ns = p.ns;
   uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ns * S::STAGE);  // A, S, x landed
+  // the partial tiles that the other CTAs of the cluster send to rank 0
+  float* cscratch = reinterpret_cast<float*>(smem + (size_t)ns * S::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ns * S::STAGE +
+                                               (size_t)(p.ksplit - 1) * S::SLOT);  // A, S, x landed
   uint64_t* empty = full + ns;                                                 // stage free
+  uint64_t* sent = empty + ns;  // rank 0: the other ranks' partial tiles have landed
   // Shared-memory addresses as 32-bit values; stage s starts at st0 + s * STAGE,
   // its barriers at full0 + 8 s and empty0 + 8 s.
   const uint32_t st0 = smem_u32(stages);
@@ -226,9 +232,14 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], S::CONS);
     }
+    // one arrival per lane of the k-group-0 consumer warps of every other rank
+    if (p.ksplit > 1) mbar_init(sent, (uint32_t)(p.ksplit - 1) * 4 * 32);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // The other ranks touch this CTA's barrier only after the matching cluster
+  // wait below, by which time every CTA of the cluster has initialised its own.
+  if (p.ksplit > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   const bool producer = warp == S::CONS;
   // Dependents may launch at once: another tensor-core GEMM queues its CTAs
@@ -517,37 +528,46 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     }
   }
 
-  // ---- reduce the cluster's K splits in rank order through distributed smem
+  // ---- reduce the cluster's K splits in rank order through distributed smem:
+  // each other rank's k-group-0 warps store their partial tile into rank 0's
+  // cscratch and arrive (release, cluster scope) on rank 0's `sent` barrier;
+  // rank 0 waits for the phase (acquire, cluster scope) and adds the partials
+  // in rank order. No rank waits for another except rank 0 for the partials,
+  // and no CTA's shared memory is written after that CTA has been waited for.
   if (p.ksplit > 1) {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (!producer && kj == 0 && rank != 0) {
-      const uint32_t local = smem_u32(stages) +
-                             (uint32_t)(((rank - 1) * 4 * 32 + mi * 32 + lane) * S::NF * 4);
-      uint32_t remote;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(0));
-      int q = 0;
-#pragma unroll
-      for (int m = 0; m < S::NMAT; ++m)
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote + 4 * q), "f"(acc[m][n][e])
-                         : "memory");
-            ++q;
-          }
-    }
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (!producer && kj == 0 && rank == 0) {
-      for (int r = 1; r < p.ksplit; ++r) {
-        const float* srcp = scratch + (size_t)(((r - 1) * 4 * 32) + mi * 32 + lane) * S::NF;
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every `sent` initialised
+    if (!producer && kj == 0) {
+      if (rank != 0) {
+        const uint32_t local = smem_u32(cscratch) +
+                               (uint32_t)(((rank - 1) * 4 * 32 + mi * 32 + lane) * S::NF * 4);
+        uint32_t remote, rbar;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(0));
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(smem_u32(sent)), "r"(0));
         int q = 0;
 #pragma unroll
         for (int m = 0; m < S::NMAT; ++m)
 #pragma unroll
           for (int n = 0; n < NT; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[m][n][e] += srcp[q++];
+            for (int e = 0; e < 4; ++e) {
+              asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote + 4 * q), "f"(acc[m][n][e])
+                           : "memory");
+              ++q;
+            }
+        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
+                     : "memory");
+      } else {
+        mbar_wait_cluster(smem_u32(sent), 0, &g_tc_error);
+        for (int r = 1; r < p.ksplit; ++r) {
+          const float* srcp = cscratch + (size_t)(((r - 1) * 4 * 32) + mi * 32 + lane) * S::NF;
+          int q = 0;
+#pragma unroll
+          for (int m = 0; m < S::NMAT; ++m)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[m][n][e] += srcp[q++];
+        }
       }
     }
   }
@@ -629,14 +649,17 @@ TcConfig pick_config_budget(int rows, int k, size_t budget, const int (&cap)[9])
   while (ks > 1 && (ks > units || ntile > cap[ks])) --ks;
   for (; ks >= 1; --ks) {
     const int nu_max = (units + ks - 1) / ks;
-    int ns = (int)((budget - 1024) / (S::STAGE + 2 * sizeof(uint64_t)));
-    if (ns > 8) ns = 8;
-    if (ns > nu_max) ns = nu_max;
+    // Shared memory: 1 KB of alignment slack, the ring, the partial tiles that
+    // the other ranks of the cluster send to rank 0 (the k-group partials
+    // reuse the ring), and 2 ns + 1 mbarriers.
+    const size_t cscr = (size_t)(ks - 1) * S::SLOT;
+    auto need = [&](int n) { return 1024 + (size_t)n * S::STAGE + cscr + (2 * (size_t)n + 1) * 8; };
+    int ns = nu_max < 8 ? nu_max : 8;
+    while (ns >= 1 && need(ns) > budget) --ns;
     if (ns < 2 && nu_max >= 2) continue;
     if (ns < 1) continue;
-    const size_t reuse = (size_t)ns * S::STAGE;  // k-group and cluster partials reuse the ring
-    if ((size_t)(S::KG - 1) * S::SLOT > reuse || (size_t)(ks - 1) * S::SLOT > reuse) continue;
-    return TcConfig{ks, ns, 1024 + reuse + 2 * ns * sizeof(uint64_t)};
+    if ((long long)ns * S::STAGE < (long long)(S::KG - 1) * S::SLOT) continue;
+    return TcConfig{ks, ns, need(ns)};
   }
   return TcConfig{0, 0, 0};
 }
