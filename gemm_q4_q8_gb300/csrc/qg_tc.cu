@@ -163,17 +163,15 @@ struct TcParams {
 
 // KG k-groups of consumer warps split a unit's 8 blocks (8 / KG blocks per warp
 // and unit); 4 m-tiles x KG k-groups of consumers plus one TMA producer warp.
-// The single-matrix 1-8-column plan uses one k-group: four consumer warps, each
-// with one m-tile across the whole unit (fewer per-stage waits and address
-// work per weight, eight independent blocks per warp; small matrices ran 5%
-// faster). The 16-column and fused plans keep two k-groups: one k-group
-// measured no faster there and spilled in the fused plan. (Four k-groups, 16
-// consumer warps with half the work each, measured slower: every warp pays the
-// per-stage overhead. Two units per stage behind one pair of barriers measured
-// no faster.)
+// Two k-groups, measured against the alternatives: one k-group of four warps,
+// each an m-tile across the whole unit, is slower (Q4_0 5120 x 5120 at one
+// column 7.3 -> 6.9 us, twins 17408 x 5120 11.8 -> 11.4 us with two); four
+// k-groups, 16 consumer warps with half the work each, are slower too (every
+// warp pays the per-stage overhead); two units per stage behind one pair of
+// barriers are no faster.
 template <int QT, int NT, bool DUAL>
 struct TcShape {
-  static constexpr int KG = (NT == 1 && !DUAL) ? 1 : 2;
+  static constexpr int KG = 2;
   static constexpr int BPW = 8 / KG;                     // blocks per warp and unit
   static constexpr int CONS = 4 * KG;                    // consumer warps
   static constexpr int THREADS = (CONS + 1) * 32;        // + the producer warp (last)
