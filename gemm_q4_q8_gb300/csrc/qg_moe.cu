@@ -48,6 +48,8 @@ constexpr int MOE_MAXJ = 17;               // topk + shared
 constexpr int MOE_XSMEM_FLOATS = 32768;    // staged activations per CTA (128 KB)
 static_assert(MOE_MAXN <= MOE_THREADS, "one id-list slot per thread");
 
+__device__ int32_t g_moe_error = 0;  // QG_DEV_ERR_WAIT: a wait timed out
+
 struct MoeDev {
   const uint8_t *qg, *qu, *qd;
   const uint16_t *sg, *su, *sd;
@@ -118,14 +120,83 @@ __device__ __forceinline__ MoeK1Rows<QT> moe_k1_rows(const MoeDev& p, const int1
   return w;
 }
 
+// The pair order of K1, shared by both gate/up kernels: every thread of the
+// CTA calls this after the kernel's wait. x is staged (f32, consumption order
+// of QT) into xs while the ids load; the valid (column, k) positions are
+// ranked by (expert id, position) into s_order / s_pc / s_pj, followed by the
+// shared expert's columns (codes n + c). CTA 0 also writes the distinct ids
+// and the bad-id bit. Returns the number of pairs.
+struct MoePairSmem {
+  int ids[MOE_MAXN];
+  __align__(16) int key[MOE_MAXN];     // id * MOE_MAXN + position, or INT_MAX
+  int16_t order[MOE_MAXN + MOE_MAXC];  // routed pairs, then the shared expert's
+  int8_t pc[MOE_MAXN + MOE_MAXC], pj[MOE_MAXN + MOE_MAXC];  // column, k slot
+};
+
+template <int QT>
+__device__ __forceinline__ int moe_pair_order(const MoeDev& p, MoePairSmem& sm, float* xs) {
+  const int n = p.ncols * p.topk;
+  const int t = threadIdx.x;
+  const int k = p.hidden;
+  // The ids are loaded first; x is staged while they are in flight.
+  int id = -1;
+  if (t < n) id = p.ids[t];
+  stage_x_cols(QT, xs, k, p.x, (size_t)k, p.ncols, k);
+  bool valid = false;
+  if (t < n) {
+    valid = id >= 0 && id < p.n_expert;
+    sm.ids[t] = valid ? id : -1;
+  }
+  if (t < MOE_MAXN) sm.key[t] = valid ? id * MOE_MAXN + t : 0x7fffffff;
+  const int nvalid = __syncthreads_count(valid);  // also publishes the staged x
+  if (valid) {
+    // rank = number of keys below this one (keys are distinct)
+    const int key = id * MOE_MAXN + t;
+    const int4* k4 = reinterpret_cast<const int4*>(sm.key);
+    int rank = 0;
+#pragma unroll 4
+    for (int s = 0; s < (n + 3) / 4; ++s) {
+      const int4 o = k4[s];
+      rank += (o.x < key) + (o.y < key) + (o.z < key) + (o.w < key);
+    }
+    sm.order[rank] = (int16_t)t;
+    sm.pc[rank] = (int8_t)(t / p.topk);
+    sm.pj[rank] = (int8_t)(t % p.topk);
+  }
+  if (p.has_shared && t < p.ncols) {
+    sm.order[nvalid + t] = (int16_t)(n + t);
+    sm.pc[nvalid + t] = (int8_t)t;
+    sm.pj[nvalid + t] = (int8_t)p.topk;
+  }
+  __syncthreads();
+
+  if (blockIdx.x == 0) {
+    // distinct valid ids, ascending, padded with -1; error bit for bad ids
+    bool start = false;
+    int cur = -1;
+    if (t < nvalid) {
+      cur = sm.ids[sm.order[t]];
+      start = t == 0 || sm.ids[sm.order[t - 1]] != cur;
+    }
+    const int U = __syncthreads_count(start);
+    if (p.uniq_out) {
+      if (start) {
+        int u = 0;
+        for (int r = 1; r <= t; ++r) u += sm.ids[sm.order[r]] != sm.ids[sm.order[r - 1]] ? 1 : 0;
+        p.uniq_out[u] = cur;
+      }
+      if (t >= U && t < n) p.uniq_out[t] = -1;
+    }
+    if (t == 0 && nvalid < n && p.err_flag) atomicOr(p.err_flag, (int32_t)QG_MOE_BAD_ID);
+  }
+  return nvalid + (p.has_shared ? p.ncols : 0);
+}
+
 // WARPS: 8, or 16 when the staged x is too large for two CTAs per SM (one
 // CTA of 16 warps then keeps as many rows in flight as two of 8).
 template <int QT, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) moe_gate_up_kernel(const MoeDev p) {
-  __shared__ int s_ids[MOE_MAXN];
-  __shared__ __align__(16) int s_key[MOE_MAXN];   // id * MOE_MAXN + position, or INT_MAX
-  __shared__ int16_t s_order[MOE_MAXN + MOE_MAXC];   // routed pairs, then the shared expert's
-  __shared__ int8_t s_pc[MOE_MAXN + MOE_MAXC], s_pj[MOE_MAXN + MOE_MAXC];  // column, k slot
+  __shared__ MoePairSmem sm;
   extern __shared__ float4 smem_f4[];
   float* xs = reinterpret_cast<float*>(smem_f4);
   constexpr int QB = QTraits<QT>::QB;
@@ -137,62 +208,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) moe_gate_up_ke
   // kernel that wrote them has completed.
   pdl_wait();  // ids and x come from earlier kernels on the stream
   pdl_trigger();
-
-  // The ids are loaded first; x is staged while they are in flight.
-  int id = -1;
-  if (t < n) id = p.ids[t];
-  stage_x_cols(QT, xs, k, p.x, (size_t)k, p.ncols, k);
-
-  // Pair order: valid positions by (expert id, position), then the shared
-  // expert's columns (codes n + c).
-  bool valid = false;
-  if (t < n) {
-    valid = id >= 0 && id < p.n_expert;
-    s_ids[t] = valid ? id : -1;
-  }
-  if (t < MOE_MAXN) s_key[t] = valid ? id * MOE_MAXN + t : 0x7fffffff;
-  const int nvalid = __syncthreads_count(valid);  // also publishes the staged x
-  if (valid) {
-    // rank = number of keys below this one (keys are distinct)
-    const int key = id * MOE_MAXN + t;
-    const int4* k4 = reinterpret_cast<const int4*>(s_key);
-    int rank = 0;
-#pragma unroll 4
-    for (int s = 0; s < (n + 3) / 4; ++s) {
-      const int4 o = k4[s];
-      rank += (o.x < key) + (o.y < key) + (o.z < key) + (o.w < key);
-    }
-    s_order[rank] = (int16_t)t;
-    s_pc[rank] = (int8_t)(t / p.topk);
-    s_pj[rank] = (int8_t)(t % p.topk);
-  }
-  if (p.has_shared && t < p.ncols) {
-    s_order[nvalid + t] = (int16_t)(n + t);
-    s_pc[nvalid + t] = (int8_t)t;
-    s_pj[nvalid + t] = (int8_t)p.topk;
-  }
-  __syncthreads();
-  const int P = nvalid + (p.has_shared ? p.ncols : 0);
-
-  if (blockIdx.x == 0) {
-    // distinct valid ids, ascending, padded with -1; error bit for bad ids
-    bool start = false;
-    int cur = -1;
-    if (t < nvalid) {
-      cur = s_ids[s_order[t]];
-      start = t == 0 || s_ids[s_order[t - 1]] != cur;
-    }
-    const int U = __syncthreads_count(start);
-    if (p.uniq_out) {
-      if (start) {
-        int u = 0;
-        for (int r = 1; r <= t; ++r) u += s_ids[s_order[r]] != s_ids[s_order[r - 1]] ? 1 : 0;
-        p.uniq_out[u] = cur;
-      }
-      if (t >= U && t < n) p.uniq_out[t] = -1;
-    }
-    if (t == 0 && nvalid < n && p.err_flag) atomicOr(p.err_flag, (int32_t)QG_MOE_BAD_ID);
-  }
+  const int P = moe_pair_order<QT>(p, sm, xs);
 
   const int lane = t & 31, warp = t >> 5;
   const int nb = k / QK;
@@ -205,8 +221,8 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) moe_gate_up_ke
   int item = blockIdx.x * WARPS + warp;
 
   for (; item < total; item += stride) {
-    const MoeK1Rows<QT> cur = moe_k1_rows<QT>(p, s_order, s_ids, s_pc, s_pj, n, item / ngroups,
-                                              item % ngroups, mat_q, mat_s);
+    const MoeK1Rows<QT> cur = moe_k1_rows<QT>(p, sm.order, sm.ids, sm.pc, sm.pj, n,
+                                              item / ngroups, item % ngroups, mat_q, mat_s);
     float ta[MOE_RW1], tb[MOE_RW1];
 #pragma unroll
     for (int r = 0; r < MOE_RW1; ++r) { ta[r] = 0.f; tb[r] = 0.f; }
@@ -348,8 +364,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_down_kernel(const MoeDev p
 // Dynamic shared memory: h of the live entries as f32 planes [nj][ffn], then
 // per entry its R rows of quants [R][ffn/32 * QB] and of scales
 // [R][ffn/32] (padded to 16 bytes).
-__device__ int32_t g_moe_error = 0;  // QG_DEV_ERR_WAIT: a wait timed out
-
 template <int QT>
 __global__ void __launch_bounds__(MOE_THREADS, 2) moe_down_staged_kernel(const MoeDev p, int R) {
   __shared__ int s_e[MOE_MAXJ];     // expert of each live entry (n_expert = shared)
@@ -486,7 +500,7 @@ bool moe_shape_supported(int ffn, int hidden, int ncols, int topk) {
 
 template <class K>
 static cudaError_t launch_moe(K kern, int threads, long grid_max_units, int multiple, size_t smem,
-                              const MoeDev& d, cudaStream_t s) {
+                              const MoeDev& d, cudaStream_t s, LaunchClass cls) {
   int occ = 1;
   cudaError_t e = kernel_occupancy(reinterpret_cast<const void*>(kern), threads, smem, &occ);
   if (e != cudaSuccess) return e;
@@ -494,7 +508,7 @@ static cudaError_t launch_moe(K kern, int threads, long grid_max_units, int mult
   if (grid > grid_max_units) grid = grid_max_units;
   grid = grid / multiple * multiple;
   if (grid < multiple) grid = multiple;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3((unsigned)threads), smem, s, 0, LC_L1, d);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3((unsigned)threads), smem, s, 0, cls, d);
 }
 
 template <int QT>
@@ -504,9 +518,16 @@ static cudaError_t moe_launch_t(const MoeDev& d, cudaStream_t s) {
   const size_t smem_gu = (size_t)d.ncols * d.hidden * sizeof(float);
   cudaError_t e;
   if (smem_gu <= 100 * 1024) {
-    e = launch_moe(moe_gate_up_kernel<QT, 8>, 256, (pairs_max * ngroups + 7) / 8, 1, smem_gu, d, s);
+    e = launch_moe(moe_gate_up_kernel<QT, 8>, 256, (pairs_max * ngroups + 7) / 8, 1, smem_gu, d, s,
+                   LC_L1);
   } else {
-    e = launch_moe(moe_gate_up_kernel<QT, 16>, 512, (pairs_max * ngroups + 15) / 16, 1, smem_gu, d, s);
+    // One CTA per SM holding more than 100 KB of shared memory: launched as
+    // LC_SMEM, so the register down kernel does not start on its SMs (16
+    // columns, 256 experts, ffn 512, hidden 2048: 84.9 -> 82.4 us per layer
+    // call; as LC_SMEM the 8-warp variant measured slower, 47.8 -> 48.7 us at
+    // 8 columns).
+    e = launch_moe(moe_gate_up_kernel<QT, 16>, 512, (pairs_max * ngroups + 15) / 16, 1, smem_gu, d, s,
+                   LC_SMEM);
   }
   if (e != cudaSuccess) return e;
   size_t smem_ds = 0;
@@ -525,8 +546,9 @@ static cudaError_t moe_launch_t(const MoeDev& d, cudaStream_t s) {
   const long big = 1L << 30;
   // one row per lane per item when few columns share the grid (more items,
   // all of a lane's experts in flight at once); two rows otherwise
-  if (d.ncols <= 2) return launch_moe(moe_down_kernel<QT, 1, 9>, MOE_THREADS, big, d.ncols, smem_dn, d, s);
-  return launch_moe(moe_down_kernel<QT, 2, 3>, MOE_THREADS, big, d.ncols, smem_dn, d, s);
+  if (d.ncols <= 2)
+    return launch_moe(moe_down_kernel<QT, 1, 9>, MOE_THREADS, big, d.ncols, smem_dn, d, s, LC_L1);
+  return launch_moe(moe_down_kernel<QT, 2, 3>, MOE_THREADS, big, d.ncols, smem_dn, d, s, LC_L1);
 }
 
 cudaError_t moe_device_error(int32_t* bits) {
