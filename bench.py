@@ -520,10 +520,11 @@ def run_case(args):
 # at their config sizes: greedy argmax and top-40 over one column of 248,320
 # logits; the MoE router (256 x 2048 f32, top-8) on one column; the small
 # Q8_0 decode GEMV (2048 x 2048, one column, CUDA-core kernel), which the step
-# does not contain; and a tall Q4_0 / Q8_0 matrix (--case-rows rows, default
+# does not contain; a tall Q4_0 / Q8_0 matrix (--case-rows rows, default
 # 65,536, by 5,120; --case-cols columns, default 8), where the tensor-core
-# kernel streams long enough to show its steady state.
-EXTRA_CASES = ("argmax", "topk40", "router", "q8gemv2048", "q4tall", "q8tall")
+# kernel streams long enough to show its steady state; and the MoE layer at one
+# column (the staged down kernel), cycling through its config's id sets.
+EXTRA_CASES = ("argmax", "topk40", "router", "q8gemv2048", "q4tall", "q8tall", "moe1")
 
 
 def run_extra_case(args, torch, qg):
@@ -552,6 +553,12 @@ def run_extra_case(args, torch, qg):
         fn = qg.qgemv_q4_0 if qt == synth.Q4_0 else qg.qgemv_q8_0
         for _ in range(args.steps):
             fn(q, sc, x, y, None, stream)
+    elif args.case == "moe1":
+        ct = ConfigTimer(torch, qg, None, None)
+        cfg = next(c for c in CONFIGS if c[0] == "q8_moe_c1")
+        calls = ct.build(*cfg, False)[0]
+        for i in range(args.steps):
+            calls[i % len(calls)](stream)
     elif args.case == "q8gemv2048":
         c = synth.small_q8_gemv()
         blocks = torch.from_numpy(synth.to_gguf_blocks(c["qtype"], c["q"], c["scl"])).cuda()

@@ -410,11 +410,15 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_down_staged_kernel(const M
   __syncthreads();
   const int nj = s_nj;
   const uint32_t bar = smem_u32(&s_bar);
-  if (t == 0) {
+  if (warp == 0) {
+    // lane m issues the two copies of live entry m (one instruction stream per
+    // copy pair instead of one thread issuing them all)
     const size_t mat_q = (size_t)p.hidden * rowbytes;
     const size_t mat_s = (size_t)p.hidden * nb;
-    mbar_expect_tx(bar, (uint32_t)nj * (uint32_t)nrows * (rowbytes + 2u * nb));
-    for (int m = 0; m < nj; ++m) {
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)nj * (uint32_t)nrows * (rowbytes + 2u * nb));
+    __syncwarp();
+    if (lane < nj) {
+      const int m = lane;
       const int e = s_e[m];
       const uint8_t* qe = e == p.n_expert ? p.sqd : p.qd + (size_t)e * mat_q;
       const uint16_t* se = e == p.n_expert ? p.ssd : p.sd + (size_t)e * mat_s;
@@ -445,15 +449,26 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_down_staged_kernel(const M
     const int lr = min(row - r0, nrows - 1);
     float acc = 0.f;
     for (int b = bl; b < nb; b += lpr) {
-      for (int m = 0; m < nj; ++m) {
-        const uint8_t* qp = wq + ((size_t)m * R + lr) * rowbytes + (size_t)b * QB;
-        Blk<QT> q;
-        q.load_shared(qp);
-        const uint16_t sc =
-            *reinterpret_cast<const uint16_t*>(wsc + (size_t)m * sstride + ((size_t)lr * nb + b) * 2);
-        float2 xr[16];
-        load_x16(hs + m * k, nb, b, xr);
-        acc = fmaf(s_w[m] * h2f(sc), blk_dot(q, xr), acc);
+      // three experts' blocks are read before any is used; the sum still
+      // takes the experts one at a time, in k order
+      for (int m0 = 0; m0 < nj; m0 += 3) {
+        Blk<QT> q[3];
+        uint16_t sc[3];
+#pragma unroll
+        for (int jj = 0; jj < 3; ++jj) {
+          const int m = min(m0 + jj, nj - 1);
+          q[jj].load_shared(wq + ((size_t)m * R + lr) * rowbytes + (size_t)b * QB);
+          sc[jj] = *reinterpret_cast<const uint16_t*>(wsc + (size_t)m * sstride +
+                                                      ((size_t)lr * nb + b) * 2);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 3; ++jj) {
+          if (m0 + jj < nj) {
+            float2 xr[16];
+            load_x16(hs + (m0 + jj) * k, nb, b, xr);
+            acc = fmaf(s_w[m0 + jj] * h2f(sc[jj]), blk_dot(q[jj], xr), acc);
+          }
+        }
       }
     }
     for (int off = lpr >> 1; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
