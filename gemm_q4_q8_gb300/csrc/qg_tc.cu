@@ -243,24 +243,24 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     const int lm = lane >> 3, lr = lane & 7;
     const uint32_t boff = (uint32_t)(S::AS_BYTES + (BPW * kj >> 1) * S::CPAD * 128 + lr * 128);
     const uint32_t xo0 = boff + (uint32_t)((lm ^ lr) << 4), xo1 = boff + (uint32_t)(((4 + lm) ^ lr) << 4);
+    if (!DUAL && p.y0 && kj == 0 && rank == 0 && nu > 0) {
+      // The epilogue's residual, fetched before the stream rather than after
+      // it (its DRAM round trip then overlaps the stream). It comes from an
+      // earlier kernel on the stream: wait for that kernel first. Nothing is
+      // lost by waiting here: the first stage's x follows the same wait.
+      pdl_wait();
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int row = m0 + mi * 16 + g + ((e >> 1) << 3);
+          const int col = n * 8 + 2 * t + (e & 1);
+          y0v[n][e] = (row < p.rows && col < p.ncols) ? p.y0[(size_t)col * p.rows + row] : 0.f;
+        }
+    }
     uint32_t st = st0, fb = full0, eb = empty0;
     for (int i = 0, s = 0, ph = 0; i < nu; ++i) {
       if (!mbar_wait(fb, (uint32_t)ph)) break;
-      if (i == 0 && !DUAL && p.y0 && kj == 0 && rank == 0) {
-        // The epilogue's residual, fetched now rather than after the loop (its
-        // DRAM round trip then overlaps the stream). It comes from an earlier
-        // kernel on the stream: wait for that kernel first (the first stage's x
-        // implies it has completed; the wait makes its writes visible here).
-        pdl_wait();
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int row = m0 + mi * 16 + g + ((e >> 1) << 3);
-            const int col = n * 8 + 2 * t + (e & 1);
-            y0v[n][e] = (row < p.rows && col < p.ncols) ? p.y0[(size_t)col * p.rows + row] : 0.f;
-          }
-      }
       // the BPW f16 scales of rows g and g+8 for this k-group's blocks, per matrix
       float dg[S::NMAT][BPW], dg8[S::NMAT][BPW];
 #pragma unroll
