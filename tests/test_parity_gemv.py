@@ -143,6 +143,31 @@ def test_ragged_shapes(qtype, rows, k, ncols):
     check_case(case, what=f"ragged {qtype} {rows}x{k} C={ncols}")
 
 
+# Row counts (k = 2048, 8 units of 256) whose tensor-core plan splits K over
+# 8, 7, ..., 1 CTAs: the largest cluster whose clusters all stay resident on a
+# GB300 at two CTAs per SM (36, 38, 46, 58, 74, 97, 152 clusters of 8 ... 2).
+# Every count is ragged (not a multiple of the 64-row tile) and above 2^22
+# weights, so 1-8 columns run on the tensor cores too.
+K_SPLIT_ROWS = {8: 2299, 7: 2419, 6: 2943, 5: 3682, 4: 4729, 3: 6158, 2: 9725, 1: 10257}
+
+
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+@pytest.mark.parametrize("ksplit", sorted(K_SPLIT_ROWS))
+@pytest.mark.parametrize("ncols", [1, 8, 16])
+def test_every_k_split(qtype, ksplit, ncols):
+    """Each K-split cluster size reduces its partial tiles through the one-way
+    handoff to rank 0: the result is checked against the oracle, and for 8
+    columns every column bit for bit against the 1-column call on it."""
+    rows = K_SPLIT_ROWS[ksplit]
+    case = synth.gemv_case(qtype, rows, 2048, ncols, residual=True, seed=100 + ksplit)
+    y = check_case(case, api="cols", what=f"{qtype} {rows}x2048 C={ncols} (K split {ksplit})")
+    if ncols == 8:
+        for c in range(ncols):
+            y1 = run_gemv(qtype, case["q"], case["scl"], case["x"][c:c + 1],
+                          case["y0"][c:c + 1], api="gemv")
+            assert np.array_equal(y1[0].view(np.uint32), y[c].view(np.uint32)), c
+
+
 @pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
 @pytest.mark.parametrize("ncols", list(range(1, 17)))
 def test_prefill_cols_all_widths(qtype, ncols):
