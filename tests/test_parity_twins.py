@@ -89,8 +89,12 @@ def test_gate_up_twins_bit_identical(qtype, rows, k):
             assert np.array_equal(hn[c], singles[c]), f"gate/up columns={n}: column {c}"
 
 
-def test_moe_twins_bit_identical():
-    case = synth.moe_case(synth.Q8_0, 32, 128, 512, 16, topk=4, shared=True, residual=True,
+@pytest.mark.parametrize("ffn", [128, 512])
+def test_moe_twins_bit_identical(ffn):
+    """ffn 512 runs every down kernel: the staged one (1-2 columns), the ring
+    (5-8 columns) and the register kernel (16 columns); ffn 128 the register
+    kernel throughout."""
+    case = synth.moe_case(synth.Q8_0, 32, ffn, 512, 16, topk=4, shared=True, residual=True,
                           seed=21)
     t, E, ffn, hidden = case["qtype"], case["n_expert"], case["ffn"], case["hidden"]
     mats = [dev_q(t, case[a], case[b]) for a, b in (("qg", "sg"), ("qu", "su"), ("qd", "sd"))]
@@ -110,7 +114,7 @@ def test_moe_twins_bit_identical():
         torch.cuda.synchronize()
         return host(y)
     singles = [run([c])[0] for c in range(16)]
-    for n in (2, 8, 16):
+    for n in (2, 6, 8, 16):
         yn = run(list(range(n)))
         for c in range(n):
             assert np.array_equal(yn[c].view(np.uint32), singles[c].view(np.uint32)), \
