@@ -24,13 +24,11 @@
 //                 fixed butterfly sums the lanes of a row, and
 //                 y = y0 + total is written once. The summation order depends
 //                 only on the shape, so results are identical run to run.
-//                 Three kernels compute it with the same arithmetic: for one or
+//                 Two kernels compute it with the same arithmetic: for one or
 //                 two columns the CTA's row slices of all its down matrices
 //                 are staged in shared memory by bulk copies issued before the
-//                 kernel waits on K1; for 5-8 columns (ffn 512 or 1,024) the
-//                 slices of one expert at a time stream through a ring of
-//                 stages; otherwise each lane streams its blocks through
-//                 registers.
+//                 kernel waits on K1; otherwise each lane streams its blocks
+//                 through registers.
 // An id outside [0, E) contributes nothing and sets a bit in the caller's error
 // word; no trap is raised and no CTA waits on another.
 #include <cuda_runtime.h>
@@ -481,152 +479,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 2) moe_down_staged_kernel(const M
   }
 }
 
-// ---------------------------------------- K2r: down + combine, ring-staged
-// For ffn of at most 1,024 (one block per lane) and more than two columns. A
-// CTA owns one column and MOE_RING_ROWS output rows; its producer warp brings
-// the rows' slice of one down matrix at a time -- the live entries in k order,
-// the shared expert last -- into a ring of stages by bulk copies (reading the
-// ids before the kernel's dependency wait, see K2s), and the eight consumer
-// warps add each expert's blocks to their rows' running sums. With one block
-// per lane the sum is the one moe_down_kernel and K2s compute (per lane, the
-// experts of its block in k order, then the same butterfly), so all three give
-// bit-identical outputs.
-constexpr int MOE_RING_ROWS = 64;
-constexpr int MOE_RING_NS = 2;
-constexpr int MOE_RING_THREADS = MOE_THREADS + 32;  // + the producer warp
-
-template <int QT>
-__global__ void __launch_bounds__(MOE_RING_THREADS, 2) moe_down_ring_kernel(const MoeDev p) {
-  __shared__ int s_e[MOE_MAXJ];     // expert of each live entry (n_expert = shared)
-  __shared__ int s_j[MOE_MAXJ];     // its position j (h index)
-  __shared__ float s_w[MOE_MAXJ];   // its routing weight
-  __shared__ int s_nj;
-  __shared__ __align__(8) uint64_t s_full[MOE_RING_NS], s_empty[MOE_RING_NS];
-  extern __shared__ float4 smem_f4[];
-  constexpr int QB = QTraits<QT>::QB;
-  constexpr int R = MOE_RING_ROWS;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int k = p.ffn, nb = k / QK;
-  const int njmax = p.topk + (p.has_shared ? 1 : 0);
-  const uint32_t rowbytes = (uint32_t)nb * QB;
-  const uint32_t qbytes = R * rowbytes;
-  const uint32_t sbytes = (uint32_t)((R * nb * 2 + 15) & ~15);
-  const uint32_t stage = qbytes + sbytes;
-  // layout: [h: njmax x ffn f32 planes][ring: MOE_RING_NS stages of quants + scales]
-  float* hs = reinterpret_cast<float*>(smem_f4);
-  uint8_t* ring = reinterpret_cast<uint8_t*>(hs + (size_t)njmax * k);
-  pdl_trigger();
-  const int c = blockIdx.x % p.ncols, part = blockIdx.x / p.ncols;
-  const int r0 = part * R;
-  const int nrows = min(R, p.hidden - r0);  // a multiple of 8 (hidden % 32 == 0)
-  if (warp == 0) {
-    int id = -1;
-    float w = 0.f;
-    if (lane < p.topk) {
-      id = p.ids[c * p.topk + lane];
-      w = p.rw[c * p.topk + lane];
-    }
-    const bool live = lane < p.topk && id >= 0 && id < p.n_expert;
-    const unsigned m = __ballot_sync(0xffffffffu, live);
-    if (live) {
-      const int at = __popc(m & ((1u << lane) - 1u));
-      s_e[at] = id; s_j[at] = lane; s_w[at] = w;
-    }
-    const int nl = __popc(m);
-    if (lane == 0) {
-      if (p.has_shared) { s_e[nl] = p.n_expert; s_j[nl] = p.topk; s_w[nl] = 1.f; }
-      s_nj = nl + (p.has_shared ? 1 : 0);
-      for (int i = 0; i < MOE_RING_NS; ++i) {
-        mbar_init(&s_full[i], 1);
-        mbar_init(&s_empty[i], MOE_WARPS);
-      }
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-  }
-  __syncthreads();
-  const int nj = s_nj;
-  const uint32_t full0 = smem_u32(s_full), empty0 = smem_u32(s_empty), ring0 = smem_u32(ring);
-
-  if (warp == MOE_WARPS) {
-    // producer: expert m's rows [r0, r0 + nrows) into stage m % MOE_RING_NS
-    if (lane == 0) {
-      const size_t mat_q = (size_t)p.hidden * rowbytes;
-      const size_t mat_s = (size_t)p.hidden * nb;
-      for (int m = 0, s = 0, ph = 0; m < nj; ++m) {
-        if (m >= MOE_RING_NS && !mbar_wait(empty0 + 8 * s, (uint32_t)(ph ^ 1), &g_moe_error)) break;
-        const int e = s_e[m];
-        const uint8_t* qe = e == p.n_expert ? p.sqd : p.qd + (size_t)e * mat_q;
-        const uint16_t* se = e == p.n_expert ? p.ssd : p.sd + (size_t)e * mat_s;
-        const uint32_t st = ring0 + (uint32_t)s * stage, fb = full0 + 8 * s;
-        mbar_expect_tx(fb, (uint32_t)nrows * (rowbytes + 2u * nb));
-        bulk_g2s(st, qe + (size_t)r0 * rowbytes, (uint32_t)nrows * rowbytes, fb);
-        bulk_g2s(st + qbytes, se + (size_t)r0 * nb, (uint32_t)nrows * nb * 2u, fb);
-        if (++s == MOE_RING_NS) { s = 0; ph ^= 1; }
-      }
-    }
-    __syncwarp();
-    return;
-  }
-
-  // consumers: h of the live entries as f32 planes (entry m at hs + m * k)
-  pdl_wait();  // the gate/up results, and y0, come from earlier kernels
-  for (int it = t; it < nj * nb; it += MOE_THREADS) {
-    const int m = it / nb, b = it % nb;
-    stage_block(QT, hs + m * k, nb, b,
-                p.hws + ((size_t)c * (p.topk + 1) + s_j[m]) * k + (size_t)b * QK);
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(MOE_THREADS) : "memory");
-
-  // The lanes of a warp split into rpw groups of lpr lanes (lpr = nb: 16 or
-  // 32); a group takes one row, lane bl of it the row's block bl. Item i of
-  // warp w is the rpw rows (w + 8 i) * rpw + group.
-  const int lpr = nb;
-  const int rpw = 32 / lpr;
-  const int rs = lane / lpr, bl = lane % lpr;
-  constexpr int MAXI = R / MOE_WARPS;        // items per warp when rpw = 1
-  const int nitem = R / (rpw * MOE_WARPS);    // 8 or 4
-  float acc[MAXI];
-#pragma unroll
-  for (int i = 0; i < MAXI; ++i) acc[i] = 0.f;
-  for (int m = 0, s = 0, ph = 0; m < nj; ++m) {
-    mbar_wait(full0 + 8 * s, (uint32_t)ph, &g_moe_error);
-    const uint8_t* st = ring + (size_t)s * stage;
-    const float wm = s_w[m];
-    float2 xr[16];
-    load_x16(hs + m * k, nb, bl, xr);
-#pragma unroll
-    for (int i = 0; i < MAXI; ++i) {
-      if (i < nitem) {
-        const int lr = min((warp + MOE_WARPS * i) * rpw + rs, nrows - 1);
-        Blk<QT> q;
-        q.load_shared(st + (size_t)lr * rowbytes + (size_t)bl * QB);
-        const uint16_t sc =
-            *reinterpret_cast<const uint16_t*>(st + qbytes + ((size_t)lr * nb + bl) * 2);
-        acc[i] = fmaf(wm * h2f(sc), blk_dot(q, xr), acc[i]);
-      }
-    }
-    // release after the arithmetic: every value read from the stage feeds the
-    // sums, which the empty asm pins before the arrive
-#pragma unroll
-    for (int i = 0; i < MAXI; ++i) asm volatile("" ::"f"(acc[i]));
-    __syncwarp();
-    mbar_arrive_lane0(empty0 + 8 * s, lane);
-    if (++s == MOE_RING_NS) { s = 0; ph ^= 1; }
-  }
-#pragma unroll
-  for (int i = 0; i < MAXI; ++i) {
-    if (i < nitem) {
-      float v = acc[i];
-      for (int off = lpr >> 1; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      const int row = r0 + (warp + MOE_WARPS * i) * rpw + rs;
-      if (bl == 0 && row < r0 + nrows) {
-        const size_t o = (size_t)c * p.hidden + row;
-        p.y[o] = (p.y0 ? p.y0[o] : 0.f) + v;
-      }
-    }
-  }
-}
-
 // Rows per CTA of the staged down kernel for this call, or 0 when the register
 // kernel runs instead: for more than two columns (measured at 256 experts,
 // ffn 512, hidden 2048, top-8 + shared: 1 column 14.3 -> 12.1 us per layer
@@ -645,22 +497,6 @@ static int moe_staged_rows(int qt, int ffn, int hidden, int ncols, int topk, int
   if (need > 100 * 1024) return 0;
   *smem = need;
   return R;
-}
-
-// Dynamic shared memory of the ring-staged down kernel for this call, or 0 when
-// another kernel runs: outside 5-8 columns (fewer columns leave most SMs
-// without a CTA; at 1-2 the staged kernel runs; at 16 columns, 512 CTAs in
-// two waves, the ring kernel measured 82.6 -> 85.0 us per layer call against
-// the register kernel, at 8 columns 47.8 -> 45.3), ffn other than 512 or
-// 1,024 (one block per lane needs 16 or 32 blocks a row), or no room for h
-// and the ring at two CTAs per SM.
-static size_t moe_ring_smem(int qt, int ffn, int ncols, int topk, int has_shared) {
-  const int nb = ffn / QK;
-  if (ncols < 5 || ncols > 8 || (nb != 16 && nb != 32)) return 0;
-  const size_t rowbytes = (size_t)nb * (qt == T_Q4_0 ? 16 : 32);
-  const size_t stage = MOE_RING_ROWS * rowbytes + ((MOE_RING_ROWS * nb * 2 + 15) & ~(size_t)15);
-  const size_t need = (size_t)(topk + (has_shared ? 1 : 0)) * ffn * 4 + MOE_RING_NS * stage;
-  return need <= 100 * 1024 ? need : 0;
 }
 
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -711,16 +547,6 @@ static cudaError_t moe_launch_t(const MoeDev& d, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   size_t smem_ds = 0;
   const int R = moe_staged_rows(QT, d.ffn, d.hidden, d.ncols, d.topk, d.has_shared, &smem_ds);
-  const size_t smem_ring = moe_ring_smem(QT, d.ffn, d.ncols, d.topk, d.has_shared);
-  if (smem_ring > 0) {
-    auto kern = moe_down_ring_kernel<QT>;
-    if ((e = prepare_kernel(reinterpret_cast<const void*>(kern), smem_ring, false)) != cudaSuccess)
-      return e;
-    const int parts = (d.hidden + MOE_RING_ROWS - 1) / MOE_RING_ROWS;
-    // LC_SMEM: 86 KB of shared memory per CTA (as LC_L1: 46.7 us at 8 columns)
-    return launch_pdl(kern, dim3((unsigned)(parts * d.ncols)), dim3(MOE_RING_THREADS), smem_ring,
-                      s, 0, LC_SMEM, d);
-  }
   if (R > 0) {
     auto kern = moe_down_staged_kernel<QT>;
     if ((e = prepare_kernel(reinterpret_cast<const void*>(kern), smem_ds, false)) != cudaSuccess)

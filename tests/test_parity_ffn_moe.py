@@ -165,22 +165,6 @@ def test_moe_two_columns_no_shared():
     check_moe(case, ids=ids, what="MoE Q4_0, 2 columns, no shared expert")
 
 
-def test_moe_ring_down_kernel():
-    """5-8 columns with ffn 512 or 1,024: the down projection streams one
-    expert's row slices at a time through a ring of shared-memory stages.
-    Q4_0 with ffn 1,024 (one row per 32 lanes), a ragged last row slice, a
-    residual and an out-of-range id; Q8_0 with ffn 512 (two rows per warp) and
-    no shared expert."""
-    case = synth.moe_case(synth.Q4_0, 20, 1024, 352, 6, topk=4, shared=True, residual=True,
-                          seed=31)
-    ids = case["ids"].copy()
-    ids[2, 1] = 20
-    check_moe(case, ids=ids, what="MoE Q4_0 ffn 1024, 6 columns (ring)")
-    case = synth.moe_case(synth.Q8_0, 24, 512, 192, 5, topk=6, shared=False, residual=True,
-                          seed=32)
-    check_moe(case, what="MoE Q8_0 ffn 512, 5 columns, no shared (ring)")
-
-
 @pytest.mark.parametrize("ncols", [1, 3])
 def test_moe_wide_ffn(ncols):
     """ffn 1024 with top-8 and a shared expert: the down projection's row slices

@@ -91,9 +91,8 @@ def test_gate_up_twins_bit_identical(qtype, rows, k):
 
 @pytest.mark.parametrize("ffn", [128, 512])
 def test_moe_twins_bit_identical(ffn):
-    """ffn 512 runs every down kernel: the staged one (1-2 columns), the ring
-    (5-8 columns) and the register kernel (16 columns); ffn 128 the register
-    kernel throughout."""
+    """ffn 512 runs both down kernels: the staged one (1-2 columns) and the
+    register kernel (more columns); ffn 128 the register kernel throughout."""
     case = synth.moe_case(synth.Q8_0, 32, ffn, 512, 16, topk=4, shared=True, residual=True,
                           seed=21)
     t, E, ffn, hidden = case["qtype"], case["n_expert"], case["ffn"], case["hidden"]
