@@ -13,7 +13,8 @@
 // first-ranked element, and any reduction order gives the same answer.
 //
 // GB300 design: a column is read by a cluster of 16 CTAs, each over its share
-// with two rounds of 8 independent loads per thread in flight.
+// with 8 independent loads per thread in flight (float4 when the column
+// allows, else two rounds of scalar loads).
 //  * argmax: warp, CTA and then cluster maximum of the keys (distributed shared
 //    memory, read by the rank-0 CTA).
 //  * top-k (k <= 256), 16 CTAs per column: each CTA reads its chunk once
@@ -81,6 +82,10 @@ __device__ __forceinline__ void chunk_of(int n, uint32_t rank, int parts, int& l
 }
 
 // ------------------------------------------------------------------ argmax
+// V4: float4 loads (every column starts on a 16-byte boundary and n % 4 == 0;
+// the CTAs' shares are then multiples of 4 elements): one round of 8 float4
+// per thread covers 16,384 elements per CTA.
+template <bool V4>
 __global__ void __launch_bounds__(SMP_THREADS) argmax_kernel(const float* __restrict__ x, int n,
                                                              int32_t* idx_out, float* val_out) {
   __shared__ uint64_t s_warp[SMP_THREADS / 32];
@@ -92,28 +97,53 @@ __global__ void __launch_bounds__(SMP_THREADS) argmax_kernel(const float* __rest
   pdl_wait();  // the logits come from an earlier kernel on the stream
   const float* col = x + (size_t)c * n;
   int lo, hi;
-  chunk_of(n, rank, AMX_CLUSTER, lo, hi);
   uint64_t best = 0;
-  float v[SMP_E];
+  if (V4) {
+    const int per = (((n + AMX_CLUSTER - 1) / AMX_CLUSTER) + 3) & ~3;
+    lo = min(n, (int)rank * per);
+    hi = min(n, lo + per);
+    constexpr int R4 = SMP_THREADS * SMP_E * 4;  // elements per CTA per round
+    for (int base = lo; base < hi; base += R4) {
+      float4 v[SMP_E];
 #pragma unroll
-  for (int e = 0; e < SMP_E; ++e) {
-    const int i = lo + e * SMP_THREADS + t;
-    v[e] = i < hi ? __ldg(col + i) : 0.f;
-  }
-  for (int base = lo; base < hi; base += SMP_ROUND) {
-    float w[SMP_E];  // the next round's loads are in flight meanwhile
+      for (int e = 0; e < SMP_E; ++e) {
+        const int i = base + (e * SMP_THREADS + t) * 4;
+        v[e] = i < hi ? __ldg(reinterpret_cast<const float4*>(col + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int e = 0; e < SMP_E; ++e) {
+        const int i = base + (e * SMP_THREADS + t) * 4;
+        if (i < hi) {
+          best = umax64(best, rank_key(v[e].x, (uint32_t)i));
+          best = umax64(best, rank_key(v[e].y, (uint32_t)i + 1));
+          best = umax64(best, rank_key(v[e].z, (uint32_t)i + 2));
+          best = umax64(best, rank_key(v[e].w, (uint32_t)i + 3));
+        }
+      }
+    }
+  } else {
+    chunk_of(n, rank, AMX_CLUSTER, lo, hi);
+    float v[SMP_E];
 #pragma unroll
     for (int e = 0; e < SMP_E; ++e) {
-      const int i = base + SMP_ROUND + e * SMP_THREADS + t;
-      w[e] = i < hi ? __ldg(col + i) : 0.f;
+      const int i = lo + e * SMP_THREADS + t;
+      v[e] = i < hi ? __ldg(col + i) : 0.f;
     }
+    for (int base = lo; base < hi; base += SMP_ROUND) {
+      float w[SMP_E];  // the next round's loads are in flight meanwhile
 #pragma unroll
-    for (int e = 0; e < SMP_E; ++e) {
-      const int i = base + e * SMP_THREADS + t;
-      if (i < hi) best = umax64(best, rank_key(v[e], (uint32_t)i));
+      for (int e = 0; e < SMP_E; ++e) {
+        const int i = base + SMP_ROUND + e * SMP_THREADS + t;
+        w[e] = i < hi ? __ldg(col + i) : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < SMP_E; ++e) {
+        const int i = base + e * SMP_THREADS + t;
+        if (i < hi) best = umax64(best, rank_key(v[e], (uint32_t)i));
+      }
+#pragma unroll
+      for (int e = 0; e < SMP_E; ++e) v[e] = w[e];
     }
-#pragma unroll
-    for (int e = 0; e < SMP_E; ++e) v[e] = w[e];
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, off));
@@ -496,9 +526,11 @@ __global__ void __launch_bounds__(SMP_THREADS) topk_kernel(const float* __restri
 // ----------------------------------------------------------------- launch
 cudaError_t argmax_launch(const float* x, int n, int ncols, int32_t* idx, float* val,
                           cudaStream_t s) {
-  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(argmax_kernel), 0, true);
+  const bool v4 = (n % 4) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  auto kern = v4 ? argmax_kernel<true> : argmax_kernel<false>;
+  const cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), 0, true);
   if (e != cudaSuccess) return e;
-  return launch_pdl(argmax_kernel, dim3((unsigned)(ncols * AMX_CLUSTER)), dim3(SMP_THREADS), 0, s,
+  return launch_pdl(kern, dim3((unsigned)(ncols * AMX_CLUSTER)), dim3(SMP_THREADS), 0, s,
                     AMX_CLUSTER, LC_L1, x, n, idx, val);
 }
 

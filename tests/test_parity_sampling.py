@@ -86,6 +86,29 @@ def test_many_candidates(m, k):
     check(logits(248320, 2, 5, f"lanes{m}"), k)
 
 
+def test_unaligned_logits():
+    """Logits one float past a 16-byte boundary (and n % 4 == 0): the argmax
+    and top-k fall back from float4 to scalar loads and give the same answer."""
+    x = logits(248320, 2, 9, "ties")
+    buf = torch.empty(x.size + 1, dtype=torch.float32, device="cuda")
+    dx = buf[1:].view(x.shape)
+    dx.copy_(torch.from_numpy(x))
+    assert dx.data_ptr() % 16 == 4
+    idx = torch.empty(2, dtype=torch.int32, device="cuda")
+    val = torch.empty(2, dtype=torch.float32, device="cuda")
+    qg.qargmax_f32(dx, idx, val)
+    ti = torch.empty((2, 40), dtype=torch.int32, device="cuda")
+    tv = torch.empty((2, 40), dtype=torch.float32, device="cuda")
+    qg.qtopk_f32(dx, 40, ti, tv)
+    torch.cuda.synchronize()
+    ri, rv = oracle.argmax(x)
+    rti, rtv = oracle.topk(x, 40)
+    assert np.array_equal(host(idx), ri)
+    assert np.array_equal(host(val).view(np.uint32), rv.view(np.uint32))
+    assert np.array_equal(host(ti), rti)
+    assert np.array_equal(host(tv).view(np.uint32), rtv.view(np.uint32))
+
+
 def test_all_nan_and_ascending():
     check(logits(5000, 2, 3, "allnan"), 5)
     check(logits(70000, 1, 4, "ascending"), 256)
