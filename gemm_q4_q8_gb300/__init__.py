@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemm.so")
 EXPORTS = ("qg_status_str", "qgemv_q4_0", "qgemv_q8_0", "qgemm_cols", "qffn_gate_up_silu",
            "qmoe_workspace_bytes", "qmoe_experts", "qmoe_experts_noalloc", "qrepack",
            "qargmax_f32", "qtopk_f32", "qmoe_router", "qg_kernel_launches", "qg_device_error",
-           "qg_last_cuda_error", "qg_last_cuda_error_string")
+           "qg_wait_selftest", "qg_last_cuda_error", "qg_last_cuda_error_string")
 
 QG_MOE_NOALLOC_WS_BYTES = 1 << 20
 
@@ -78,6 +78,7 @@ def load(path: str | None = None):
     L.qg_kernel_launches.argtypes = []
     L.qg_kernel_launches.restype = C.c_uint64
     L.qg_device_error.argtypes = [C.POINTER(C.c_int32)]
+    L.qg_wait_selftest.argtypes = [C.POINTER(C.c_int32), vp]
     L.qg_last_cuda_error.argtypes = []
     L.qg_last_cuda_error_string.argtypes = []
     L.qg_last_cuda_error_string.restype = C.c_char_p
@@ -190,6 +191,16 @@ def qg_device_error() -> int:
     v = C.c_int32(0)
     _check("qg_device_error", load().qg_device_error(C.byref(v)))
     return int(v.value)
+
+
+def qg_wait_selftest(stream=None) -> tuple[int, int]:
+    """Run the bounded-wait self-test (about 4 s): two waits on an mbarrier
+    phase that nothing completes, CTA scope then cluster scope. Returns per
+    wait 1 if it completed, 0 if it gave up (both 0 when the bounds work);
+    each wait that gives up sets QG_DEV_ERR_WAIT in the device error word."""
+    v = (C.c_int32 * 2)()
+    _check("qg_wait_selftest", load().qg_wait_selftest(v, _stream(stream)))
+    return int(v[0]), int(v[1])
 
 
 def qrepack(qtype, gguf, rows, k, q_out, scl_out, stream=None):

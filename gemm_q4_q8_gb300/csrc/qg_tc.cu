@@ -677,7 +677,50 @@ cudaError_t tc_gemm(int qt, const void* q, const uint16_t* scl, const void* qu,
               : tc_launch<T_Q8_0, 1, false>(q, scl, qu, su, rows, k, x, ncols, y0, y, h, s);
 }
 
+// ------------------------------------------ self-test of the bounded waits
+// (diagnostic, not part of the method)
+__device__ int32_t g_wait_selftest[2];
+
+// One thread waits on phase 0 of a fresh mbarrier that nothing arrives on:
+// first with CTA scope (the form of the stage waits), then with cluster-scope
+// acquire (the form of the K-split handoff). Each wait gives up after its clock
+// bound, sets QG_DEV_ERR_WAIT in the device error word and returns false;
+// g_wait_selftest[i] records 1 if wait i completed, 0 if it gave up.
+__global__ void wait_selftest_kernel() {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    g_wait_selftest[0] = mbar_wait(smem_u32(&bar), 0) ? 1 : 0;
+    g_wait_selftest[1] = mbar_wait_cluster(smem_u32(&bar), 0, &g_tc_error) ? 1 : 0;
+  }
+}
+
 }  // namespace qg
+
+extern "C" qg_status qg_wait_selftest(int32_t* completed_out, cudaStream_t stream) {
+  if (!completed_out) return QG_ERR_NULL;
+  const int32_t unset[2] = {-1, -1};
+  cudaError_t e = cudaMemcpyToSymbolAsync(qg::g_wait_selftest, unset, sizeof(unset), 0,
+                                          cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) {
+    qg::wait_selftest_kernel<<<1, 32, 0, stream>>>();
+    e = cudaGetLastError();
+    if (e == cudaSuccess) qg::note_launch();
+  }
+  if (e == cudaSuccess)
+    e = cudaMemcpyFromSymbolAsync(completed_out, qg::g_wait_selftest, sizeof(unset), 0,
+                                  cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    qg::note_cuda_error(e);
+    return QG_ERR_CUDA;
+  }
+  return QG_OK;
+}
 
 extern "C" qg_status qg_device_error(int32_t* bits_out) {
   if (!bits_out) return QG_ERR_NULL;

@@ -269,16 +269,32 @@ uint64_t qg_kernel_launches(void);
 /* ---------------------------------------------------------------------------
  * Diagnostics: the current device's error word, read and then cleared.
  * Not part of the method. Every wait of the tensor-core kernel (on its TMA
- * data or on a free pipeline stage) is bounded (~2 s); a wait that gives up
- * sets bit QG_DEV_ERR_WAIT and the kernel returns without its result, so the
- * outputs of that call are wrong while the context stays usable. The word is
- * shared by every call on the device since the last read.
+ * data, on a free pipeline stage, or on the partial tiles of its K split) and
+ * of the staged MoE down kernel (on its bulk copies) is bounded (~2 s); a wait
+ * that gives up sets bit QG_DEV_ERR_WAIT and the kernel returns without its
+ * result, so the outputs of that call are wrong while the context stays
+ * usable. The word is shared by every call on the device since the last read.
  *  - bits_out: host pointer, receives the word (0: no error).
  *  - Synchronises the current device (a copy from a device symbol).
  *  - QG_ERR_NULL if bits_out is null, QG_ERR_CUDA if the copies fail.
  * ------------------------------------------------------------------------- */
 #define QG_DEV_ERR_WAIT 1
 qg_status qg_device_error(int32_t *bits_out);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics: a self-test of the bounded waits. Not part of the method. One
+ * thread of one CTA waits on a phase of an mbarrier that nothing completes,
+ * first with CTA scope (the form of the tensor-core kernel's stage waits), then
+ * with cluster-scope acquire (the form of its K-split handoff). Each wait gives
+ * up after its bound (~2 s), sets QG_DEV_ERR_WAIT in the device error word and
+ * returns, so the call takes about 4 s and leaves the context usable.
+ *  - completed_out: host int32[2], receives per wait 1 if it completed, 0 if it
+ *    gave up (both 0 when the bounds work).
+ *  - Enqueues on `stream` and synchronises it.
+ *  - QG_ERR_NULL if completed_out is null; QG_ERR_CUDA if the launch or a copy
+ *    fails.
+ * ------------------------------------------------------------------------- */
+qg_status qg_wait_selftest(int32_t *completed_out, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Diagnostics: the CUDA runtime error behind the latest QG_ERR_CUDA that a

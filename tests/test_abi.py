@@ -135,6 +135,11 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert lib.qg_last_cuda_error_string().decode().startswith("cudaError")
 
 
+def test_wait_selftest_null_output(lib):
+    """The self-test checks its output pointer before launching anything."""
+    assert lib.qg_wait_selftest(None, None) == qg.QG_ERR_NULL
+
+
 def test_device_error_word(lib):
     """qg_device_error: a null output is QG_ERR_NULL; without a GPU the read of
     the device word fails loudly (QG_ERR_CUDA)."""

@@ -120,6 +120,21 @@ def test_no_device_error_after_tensor_core_calls():
     assert qg.qg_device_error() == 0
 
 
+def test_bounded_waits_give_up_and_leave_the_context_usable():
+    """The self-test waits on an mbarrier phase that nothing completes, with the
+    tensor-core kernel's two wait forms (CTA scope, cluster-scope acquire). Each
+    gives up after its bound, sets the wait bit in the device error word (read
+    once, then clear), and the context runs a tensor-core call correctly right
+    after."""
+    qg.qg_device_error()  # start from a clear word
+    assert qg.qg_wait_selftest() == (0, 0)
+    assert qg.qg_device_error() & qg.QG_DEV_ERR_WAIT
+    assert qg.qg_device_error() == 0
+    case = synth.gemv_case(synth.Q4_0, 3000, 5120, 8, residual=True, seed=58)
+    check_case(case, api="cols", what="tensor-core call after the wait self-test")
+    assert qg.qg_device_error() == 0
+
+
 def test_q4_large_one_column_sampled_rows():
     """One column of a large Q4_0 matrix (the tensor-core plan), ragged row tail."""
     case = synth.gemv_case(synth.Q4_0, 20000, 5120, 1, residual=True, seed=41)

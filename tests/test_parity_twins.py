@@ -46,7 +46,7 @@ def gemv(qtype, qd, sd, x, y0):
 @pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
 @pytest.mark.parametrize("rows,k", [
     (5120, 5120),     # tensor-core plan
-    (2048, 2048),     # tensor-core plan, small
+    (2048, 2048),     # CUDA cores (small matrix)
     (17408, 5120),    # tensor-core plan, cluster split-K
     (333, 1056),      # CUDA cores (K not a multiple of 256)
     (200, 4128),      # CUDA cores, x staged in chunks for 5-8 columns
