@@ -8,8 +8,8 @@
 // and down matrices of all experts are stacked by role, and the chosen experts
 // run as one batched multiply over the stack.
 //
-// GB300 design: two persistent kernels, both reading the device id list
-// directly (no host round trip, no compaction pass of its own).
+// GB300 design: two kernels, both reading the device id list directly (no
+// host round trip, no compaction pass of its own).
 //   K1  gate/up : work items (routed pair, 2-row group). A pair is a valid
 //                 (column, k) position of the id list, or a column of the
 //                 shared expert. Pairs run in ascending expert id, so the
@@ -25,9 +25,10 @@
 //                 y = y0 + total is written once. The summation order depends
 //                 only on the shape, so results are identical run to run.
 //                 Two kernels compute it with the same arithmetic: for one or
-//                 two columns the CTA's row slices of all its down matrices
-//                 are staged in shared memory by bulk copies issued before the
-//                 kernel waits on K1; otherwise each lane streams its blocks
+//                 two columns a CTA owns 8 rows, and their slices of all its
+//                 down matrices are staged in shared memory by bulk copies
+//                 issued before the kernel waits on K1; otherwise the warps
+//                 loop over row groups and each lane streams its blocks
 //                 through registers.
 // An id outside [0, E) contributes nothing and sets a bit in the caller's error
 // word; no trap is raised and no CTA waits on another.

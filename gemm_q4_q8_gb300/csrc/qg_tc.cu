@@ -197,7 +197,7 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 
   const int mi = warp & 3, kj = warp >> 2;  // m-tile, k-group (the producer: kj == KG)
   const int g = lane >> 2, t = lane & 3;
-  float y0v[NT][4];  // the epilogue's residual (rank 0, k-group 0; loaded in the loop)
+  float y0v[NT][4];  // the epilogue's residual (rank 0, k-group 0; loaded before the loop)
   float acc[S::NMAT][NT][4];
 #pragma unroll
   for (int m = 0; m < S::NMAT; ++m)
