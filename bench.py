@@ -315,17 +315,28 @@ class GpuStep:
 
 # -------------------------------------------------------------- clocks
 class ClockSampler:
+    """SM clock, its maximum and the clock-event reasons of one GPU, read (never
+    set) from two sources at once: `nvidia-smi -lms 50` and, every ~1 ms, NVML
+    itself (libnvidia-ml, which ships with the driver), so that a timed region
+    of a few milliseconds still holds samples."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReason* bits (nvml.h) of the reasons the record keeps
+    NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                    0x40: "hw_thermal_slowdown"}
 
     def __init__(self, index: int):
         self.index = index
-        self.samples = []  # (time, sm, max, reasons set)
+        self.samples = []  # (time, sm, max, reasons set, source)
         self.proc = None
         self.thread = None
+        self.nvml_thread = None
+        self._halt = threading.Event()
 
     def start(self):
+        self.nvml_thread = threading.Thread(target=self._nvml_loop, daemon=True)
+        self.nvml_thread.start()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
@@ -333,12 +344,42 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
+        if self.proc is not None:
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
         t0 = time.time()
-        while not self.samples and time.time() - t0 < 5:
+        while (not self.samples and time.time() - t0 < 5 and
+               (self.proc is not None or self.nvml_thread.is_alive())):
             time.sleep(0.02)
+
+    def _nvml_loop(self):
+        import ctypes as C
+        try:
+            lib = C.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return
+        if lib.nvmlInit_v2() != 0:
+            return
+        try:
+            h = C.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(C.c_uint(self.index), C.byref(h)) != 0:
+                return
+            reasons_fn = (getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or
+                          getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None))
+            clock_sm = C.c_int(1)  # NVML_CLOCK_SM
+            sm, mx, rs = C.c_uint(), C.c_uint(), C.c_ulonglong()
+            if lib.nvmlDeviceGetMaxClockInfo(h, clock_sm, C.byref(mx)) != 0:
+                return
+            while not self._halt.is_set():
+                if lib.nvmlDeviceGetClockInfo(h, clock_sm, C.byref(sm)) == 0:
+                    reasons = set()
+                    if reasons_fn is not None and reasons_fn(h, C.byref(rs)) == 0:
+                        reasons = {n for bit, n in self.NVML_REASONS.items() if rs.value & bit}
+                    self.samples.append((time.time(), float(sm.value), float(mx.value), reasons,
+                                         "nvml"))
+                time.sleep(0.001)
+        finally:
+            lib.nvmlShutdown()
 
     def _read(self):
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
@@ -351,9 +392,12 @@ class ClockSampler:
             except ValueError:
                 continue
             reasons = {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}
-            self.samples.append((time.time(), sm, mx, reasons))
+            self.samples.append((time.time(), sm, mx, reasons, "nvidia-smi"))
 
     def stop(self):
+        self._halt.set()
+        if self.nvml_thread is not None:
+            self.nvml_thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -369,11 +413,13 @@ class ClockSampler:
             note = "no sample inside the timed region; nearest samples within 0.3 s"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
+                    "note": "neither nvidia-smi nor NVML answered"}
         reasons = sorted(set().union(*[s[3] for s in inside]))
         d = {"sm_mhz": statistics.median(s[1] for s in inside),
              "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
-             "samples": len(inside)}
+             "samples": len(inside),
+             "samples_by_source": {src: sum(1 for s in inside if s[4] == src)
+                                   for src in ("nvml", "nvidia-smi")}}
         if note:
             d["note"] = note
         return d
