@@ -109,6 +109,36 @@ def test_q4_lm_head_shape_all_rows():
     assert_within(got, yr, gemv_bound(S), "Q4_0 248320x5120 C=1, every row")
 
 
+@pytest.mark.parametrize("k,engine", [(5120, "tensor cores"), (5152, "CUDA cores")])
+def test_q8_matrix_beyond_2_gib(k, engine):
+    """A Q8_0 matrix whose quants span more than 2^31 bytes (420,000 rows), at
+    1 and 8 columns with a residual: byte offsets past 2 GiB on both engines
+    (K = 5152 is not a multiple of 256, so it runs on the CUDA cores). Rows are
+    sampled at the start, around the 2 GiB boundary, at the tail and at random;
+    the output starts as NaN, so every row is also checked for being written."""
+    rows = 420000
+    assert rows * k > 2 ** 31
+    g = synth.rng(k)
+    q, s = synth.draw_matrix(g, synth.Q8_0, rows, k)
+    dq, ds = dev_q(synth.Q8_0, q, s)
+    edge = 2 ** 31 // k
+    r = np.random.Generator(np.random.PCG64(5))
+    sel = np.unique(np.concatenate([np.arange(64), edge - 64 + np.arange(128),
+                                    rows - 96 + np.arange(96), r.integers(0, rows, 1024)]))
+    for ncols in (1, 8):
+        x = synth.draw_x(g, ncols, k)
+        y0 = synth.draw_y0(g, ncols, rows)
+        y = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+        qg.qgemv_q8_0(dq, ds, dev_u16_as_f16(x), y, dev(y0))
+        torch.cuda.synchronize()
+        got = host(y)
+        assert np.isfinite(got).all(), f"{engine} C={ncols}: unwritten rows"
+        yr, S = oracle.matmul(synth.Q8_0, q, s, x, y0, rows_sel=sel, nthreads=NTHREADS)
+        assert_within(got[:, sel], yr, gemv_bound(S), f"Q8_0 {rows}x{k} ({engine}) C={ncols}")
+    del dq, ds
+    torch.cuda.empty_cache()
+
+
 def test_no_device_error_after_tensor_core_calls():
     """Every tensor-core wait is bounded; none gives up on ordinary calls, so the
     device error word reads 0 afterwards (and reading clears it)."""
