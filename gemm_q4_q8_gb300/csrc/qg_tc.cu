@@ -379,19 +379,16 @@ tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       }
       scale(BPW - 1);
       if (!S::EARLY_RELEASE) {
-        // Release after the arithmetic. Every value read from the stage (quant
-        // words and x through ldmatrix, scales through ld.shared) feeds an
-        // instruction that issues before the arrive (the mma consume the words
-        // and x; the scale FMAs, pinned here by the empty asm that takes the
-        // accumulators, consume the scales), and an instruction issues only
-        // once its operands have arrived: no read of the stage is outstanding
-        // when the producer may refill it.
-#pragma unroll
-        for (int m = 0; m < S::NMAT; ++m)
-#pragma unroll
-          for (int n = 0; n < NT; ++n)
-            asm volatile("" ::"f"(acc[m][n][0]), "f"(acc[m][n][1]), "f"(acc[m][n][2]),
-                         "f"(acc[m][n][3]));
+        // Release after the arithmetic, behind the same proxy fence as the
+        // early release: the stage's reads (ldmatrix, ld.shared) are generic-
+        // proxy accesses and its refill is a TMA write (async proxy), so only
+        // the fence orders the reads before the refill. Data dependences do
+        // not: the instruction scheduler may place the arithmetic that
+        // consumes the reads after the arrive. (Measured: a build whose block
+        // scales used packed FMAs refilled stages under live reads and gave
+        // wrong, run-to-run different sums on the 16-column down projection
+        // without this fence, and correct ones with it.)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         release();
       }
     }
