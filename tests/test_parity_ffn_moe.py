@@ -17,7 +17,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import (NTHREADS, assert_within, check_moe_staged, dev, dev_q, dev_u16,
+from helpers import (NTHREADS, assert_within, check_moe_staged, dev, dev_q,
                      dev_u16_as_f16, gemv_bound, host, workspace_h)
 
 pytestmark = pytest.mark.gpu
