@@ -124,3 +124,32 @@ def test_moe_runs_bit_identical():
                             ids, rw, x, y, w, y0=y0, shared=sh)
         torch.cuda.synchronize()
         _same(outs, f"MoE C={ncols}")
+
+
+def test_step_graph_soak():
+    """The benchmark's whole step (GEMV + residual, LM head, twins, fused
+    gate/up, down with residual, MoE layer) captured in one CUDA graph and
+    replayed 3,000 times; after every replay a device-side comparison of all
+    its outputs with the first replay's, counted on the device (no host
+    synchronisation until the end)."""
+    import bench
+    gs = bench.GpuStep(bench.make_workload(0), torch)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            gs.step(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        gs.step(s)
+    g.replay()
+    torch.cuda.synchronize()
+    out = gs.dout_flat[0].view(torch.int32)
+    ref = out.clone()
+    bad = torch.zeros((), dtype=torch.int64, device="cuda")
+    for _ in range(3000):
+        g.replay()
+        bad += ((out != ref).sum() > 0).long()
+    torch.cuda.synchronize()
+    assert int(bad) == 0, f"{int(bad)} of 3000 replays differ from the first"
+    assert qg.qg_device_error() == 0 and int(gs.m_err.item()) == 0
