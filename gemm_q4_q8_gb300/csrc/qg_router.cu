@@ -11,7 +11,9 @@
 // GB300 design: one cluster of 16 CTAs. Each warp owns experts e (one at a
 // time) and computes their logits for every column in one sweep of the
 // expert's router row: 16 float4 loads per lane in flight at once, x read from
-// shared memory, f32 accumulation in a fixed lane order, then a fixed
+// shared memory (staged as f32 on the float4 sweep, so each column's four
+// values are one load with no conversion; f16 on the scalar one), f32
+// accumulation in a fixed lane order, then a fixed
 // butterfly. The column count is a template parameter (1, 2, 4, 8 or 16) so a
 // narrow call issues no instructions for columns it does not have. Lane c of
 // the warp stores the logit of column c straight into the shared memory of CTA
@@ -53,9 +55,10 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 
 // Logits of expert row wr for NC columns (lanes hold partial sums; caller
 // reduces). VEC: float4 rows (hidden % 4 == 0, 8-byte aligned x rows).
-template <int NC, bool VEC>
-__device__ __forceinline__ void rt_row(const float* __restrict__ wr, const __half* xb, int hidden,
-                                       int ncols, int lane, float (&acc)[NC]) {
+template <int NC, bool VEC, bool XF>
+__device__ __forceinline__ void rt_row(const float* __restrict__ wr, const __half* xb,
+                                       const float* xf, int hidden, int ncols, int lane,
+                                       float (&acc)[NC]) {
 #pragma unroll
   for (int c = 0; c < NC; ++c) acc[c] = 0.f;
   if (VEC) {
@@ -75,9 +78,16 @@ __device__ __forceinline__ void rt_row(const float* __restrict__ wr, const __hal
 #pragma unroll
           for (int c = 0; c < NC; ++c)
             if (NC == 1 || c < ncols) {
-              const uint2 hv = *reinterpret_cast<const uint2*>(xb + (size_t)c * hidden + k);
-              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
-              const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hv.y));
+              float2 a, b;
+              if (XF) {
+                const float4 xv = *reinterpret_cast<const float4*>(xf + (size_t)c * hidden + k);
+                a = make_float2(xv.x, xv.y);
+                b = make_float2(xv.z, xv.w);
+              } else {
+                const uint2 hv = *reinterpret_cast<const uint2*>(xb + (size_t)c * hidden + k);
+                a = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
+                b = __half22float2(*reinterpret_cast<const __half2*>(&hv.y));
+              }
               acc[c] = fmaf(wv[u].x, a.x, acc[c]);
               acc[c] = fmaf(wv[u].y, a.y, acc[c]);
               acc[c] = fmaf(wv[u].z, b.x, acc[c]);
@@ -119,13 +129,21 @@ __global__ void __launch_bounds__(RT_THREADS) router_kernel(const float* __restr
   const int e0 = (int)rank * per;
   const int e1 = min(E, e0 + per);
   pdl_wait();  // x comes from an earlier kernel on the stream
+  // staged x: f32 (converted once) on the float4 sweep, f16 on the scalar one
+  constexpr bool XF = XS && VEC;
   if (XS) {
-    __half* sx = reinterpret_cast<__half*>(rt_smem);
     const int n = ncols * hidden;
-    for (int i = t; i < n; i += RT_THREADS) sx[i] = x[i];
+    if (XF) {
+      float* sx = reinterpret_cast<float*>(rt_smem);
+      for (int i = t; i < n; i += RT_THREADS) sx[i] = __half2float(x[i]);
+    } else {
+      __half* sx = reinterpret_cast<__half*>(rt_smem);
+      for (int i = t; i < n; i += RT_THREADS) sx[i] = x[i];
+    }
     __syncthreads();
   }
   const __half* xb = XS ? reinterpret_cast<const __half*>(rt_smem) : x;
+  const float* xf = reinterpret_cast<const float*>(rt_smem);
   // lane c stores column c into CTA c's s_lg
   uint32_t dst = 0;
   if (lane < ncols)
@@ -134,7 +152,7 @@ __global__ void __launch_bounds__(RT_THREADS) router_kernel(const float* __restr
                  : "r"((uint32_t)__cvta_generic_to_shared(s_lg)), "r"((uint32_t)lane));
   for (int e = e0 + warp; e < e1; e += RT_WARPS) {
     float acc[NC];
-    rt_row<NC, VEC>(w + (size_t)e * hidden, xb, hidden, ncols, lane, acc);
+    rt_row<NC, VEC, XF>(w + (size_t)e * hidden, xb, xf, hidden, ncols, lane, acc);
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
 #pragma unroll
@@ -233,14 +251,14 @@ static cudaError_t router_go(size_t smem, const float* w, const __half* x, int E
 cudaError_t router_launch(const float* w, const uint16_t* x, int E, int hidden, int ncols,
                           int topk, float* logits, int32_t* ids, float* rw, cudaStream_t s) {
   const __half* xh = reinterpret_cast<const __half*>(x);
-  const size_t s_x = (size_t)ncols * hidden * 2;
+  const bool vec = (hidden % 4) == 0 && (reinterpret_cast<uintptr_t>(x) & 7) == 0;
+  const size_t s_x = (size_t)ncols * hidden * (vec ? 4 : 2);
   const bool xs = s_x <= RT_XS_MAX;
   // float4 rows need 16-byte row starts (w itself is 16-byte aligned) and
   // 8-byte x row starts. The choice depends on the pointers and hidden only,
   // never on the column count, so a column's logit is the same bit for bit
   // whatever the number of columns (the lane -> k order differs between the
   // float4 and scalar sweeps).
-  const bool vec = (hidden % 4) == 0 && (reinterpret_cast<uintptr_t>(x) & 7) == 0;
   if (xs && vec) {
     if (ncols == 1) return router_go<1, true, true>(s_x, w, xh, E, hidden, ncols, topk, logits, ids, rw, s);
     if (ncols <= 2) return router_go<2, true, true>(s_x, w, xh, E, hidden, ncols, topk, logits, ids, rw, s);
