@@ -570,7 +570,7 @@ def run_case(args):
 # 65,536, by 5,120; --case-cols columns, default 8), where the tensor-core
 # kernel streams long enough to show its steady state; and the MoE layer at one
 # column (the staged down kernel), cycling through its config's id sets.
-EXTRA_CASES = ("argmax", "topk40", "router", "q8gemv2048", "q4tall", "q8tall", "moe1")
+EXTRA_CASES = ("argmax", "topk40", "router", "q8gemv2048", "q4tall", "q8tall", "moe1", "moe16")
 
 
 def run_extra_case(args, torch, qg):
@@ -599,9 +599,10 @@ def run_extra_case(args, torch, qg):
         fn = qg.qgemv_q4_0 if qt == synth.Q4_0 else qg.qgemv_q8_0
         for _ in range(args.steps):
             fn(q, sc, x, y, None, stream)
-    elif args.case == "moe1":
+    elif args.case in ("moe1", "moe16"):
         ct = ConfigTimer(torch, qg, None, None)
-        cfg = next(c for c in CONFIGS if c[0] == "q8_moe_c1")
+        name = "q8_moe_c1" if args.case == "moe1" else "q8_moe_c16"
+        cfg = next(c for c in CONFIGS if c[0] == name)
         calls = ct.build(*cfg, False)[0]
         for i in range(args.steps):
             calls[i % len(calls)](stream)
